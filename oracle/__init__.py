@@ -1,0 +1,8 @@
+"""fp64 CPU oracle for fused linear cross-entropy + entropy.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the product path.
+"""
+from .flce_oracle import (IGNORE_INDEX, backward, bf16_bits_to_f64, dlogits_chunk,  # noqa: F401
+                          forward, grad_scales, label_logits, logits_chunk, objective,
+                          row_stats)

@@ -1,0 +1,220 @@
+"""fp64 CPU oracle for fused linear cross-entropy + entropy.  TEST INFRASTRUCTURE ONLY.
+
+Nothing on the product path may import this module: only the tests, the smoke
+check and the benchmark's CPU-baseline leg use it.  It shares no code with the
+CUDA library.
+
+What it computes (plain definitions, written out in fp64):
+
+* verl PR #462, "Equivalent compute logic": logits = hidden @ weight in wide
+  precision, p = softmax(logits), entropy = logsumexp(logits) - sum(p * logits),
+  and the cross-entropy of the labelled token (the page returns its negation,
+  a log-probability).
+* Liger-Kernel PR #551 (review by qingquansong): ignored tokens are left out and
+  the mean divides by the number of non-ignored tokens, for the entropy term too.
+* Liger-Kernel PR #435, "Summary" / "Changes Made": reduction 'none' returns the
+  per-token vector; the z-loss follows the same reduction.  The z-loss formula
+  is not printed; this oracle takes z_n = coef * lse_n^2 added to the loss.
+* Liger-Kernel issue #127 (troy1729, qingquansong): the Gemma-2 soft-cap is
+  applied to the logits after the matmul in three steps (divide by c, tanh,
+  multiply by c); its backward follows from the chain rule, d tanh(x)/dx =
+  1 - tanh(x)^2.
+
+Backward (closed form of the derivative of the objective
+J = sum_n gl_n * loss_n + ge_n * entropy_n, with gl/ge the upstream gradients
+after the reduction's scaling and zero on ignored rows):
+    dz_nv = gl_n * (p_nv - [v == y_n] + 2 coef lse_n p_nv) - ge_n * p_nv * (z_nv - E_p[z]_n)
+    dz'_nv = dz_nv * (1 - (z_nv / c)^2)            (soft-cap on)
+    dhidden = dz' @ weight^T,   dweight = hidden^T @ dz'
+
+Every function works over vocabulary chunks so no [N, V] array is formed for
+the large shapes.  The maximum and the sums are taken in two passes (not an
+online recurrence), so the oracle follows the definitions as written.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+IGNORE_INDEX = -100
+_REDS = ("none", "mean", "sum")
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen raw bf16 bit patterns (uint16) to float64, exactly.
+
+    A bf16 value is the upper half of an IEEE binary32, so shifting the bits
+    left by 16 gives the binary32 value, which float64 holds exactly.
+    """
+    b = np.asarray(bits, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def _cap(zp: np.ndarray, softcap: float) -> np.ndarray:
+    """Liger-Kernel issue #127: divide by c, tanh, multiply by c (off when c == 0)."""
+    if softcap == 0.0:
+        return zp
+    return softcap * np.tanh(zp / softcap)
+
+
+def _check(hidden, weight, labels, reduction, ignore_index):
+    if reduction not in _REDS:
+        raise ValueError(f"reduction must be one of {_REDS}")
+    N, H = hidden.shape
+    H2, V = weight.shape
+    if H != H2 or labels.shape != (N,):
+        raise ValueError("shape mismatch")
+    lab = np.asarray(labels, dtype=np.int64)
+    valid = lab != ignore_index
+    if np.any((lab[valid] < 0) | (lab[valid] >= V)):
+        raise ValueError("label out of range")
+    return N, H, V, lab, valid
+
+
+def logits_chunk(hidden: np.ndarray, weight: np.ndarray, v0: int, v1: int,
+                 softcap: float = 0.0) -> np.ndarray:
+    """Capped logits z[:, v0:v1] = cap(hidden @ weight[:, v0:v1]) in fp64."""
+    return _cap(hidden @ weight[:, v0:v1], softcap)
+
+
+def row_stats(hidden, weight, softcap=0.0, v_chunk=8192):
+    """Per-row log-sum-exp and softmax mean of the capped logits.
+
+    Pass 1: m_n = max_v z_nv.  Pass 2: d_n = sum_v exp(z_nv - m_n) and
+    s_n = sum_v exp(z_nv - m_n) * z_nv.  Then lse = m + log d, E_p[z] = s / d.
+    """
+    N = hidden.shape[0]
+    V = weight.shape[1]
+    m = np.full(N, -np.inf)
+    for v0 in range(0, V, v_chunk):
+        z = logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap)
+        m = np.maximum(m, z.max(axis=1))
+    d = np.zeros(N)
+    s = np.zeros(N)
+    for v0 in range(0, V, v_chunk):
+        z = logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap)
+        e = np.exp(z - m[:, None])
+        d += e.sum(axis=1)
+        s += (e * z).sum(axis=1)
+    lse = m + np.log(d)
+    ez = s / d
+    return lse, ez
+
+
+def label_logits(hidden, weight, labels, valid, softcap=0.0):
+    """z_{n, y_n} for non-ignored rows (0 elsewhere)."""
+    zy = np.zeros(hidden.shape[0])
+    idx = np.nonzero(valid)[0]
+    if idx.size:
+        zp = np.einsum("nh,hn->n", hidden[idx], weight[:, labels[idx]])
+        zy[idx] = _cap(zp, softcap)
+    return zy
+
+
+def forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
+            zloss_coef=0.0, softcap=0.0, v_chunk=8192):
+    """Loss and entropy of verl PR #462's compute logic, with the Liger options.
+
+    Returns a dict:
+      loss, entropy   -- reduced ('mean'/'sum': float; 'none': [N] arrays)
+      loss_tok, entropy_tok -- per-token values, 0 on ignored rows
+      ce_tok          -- per-token cross-entropy (0 on ignored rows); logprob = -ce
+      lse, ez         -- per-row log-sum-exp and E_p[z] for every row (saved for backward)
+      n_valid         -- number of non-ignored rows
+    """
+    hidden = np.asarray(hidden, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
+    lse, ez = row_stats(hidden, weight, softcap, v_chunk)
+    zy = label_logits(hidden, weight, lab, valid, softcap)
+    ce = np.where(valid, lse - zy, 0.0)
+    ent = np.where(valid, lse - ez, 0.0)
+    zl = np.where(valid, zloss_coef * lse * lse, 0.0)
+    loss_tok = ce + zl
+    n_valid = int(valid.sum())
+    if reduction == "none":
+        loss, entropy = loss_tok, ent
+    elif reduction == "sum":
+        loss, entropy = float(loss_tok.sum()), float(ent.sum())
+    else:
+        # mean over non-ignored tokens; an all-ignored batch reduces to 0
+        den = float(n_valid) if n_valid > 0 else None
+        loss = float(loss_tok.sum()) / den if den else 0.0
+        entropy = float(ent.sum()) / den if den else 0.0
+    return dict(loss=loss, entropy=entropy, loss_tok=loss_tok, entropy_tok=ent, ce_tok=ce,
+                lse=lse, ez=ez, n_valid=n_valid, valid=valid)
+
+
+def grad_scales(g_loss, g_entropy, valid, reduction):
+    """Per-row upstream gradients after the reduction: g (none/sum) or g / n_valid (mean),
+    zero on ignored rows."""
+    N = valid.shape[0]
+    gl = np.broadcast_to(np.asarray(g_loss, dtype=np.float64).reshape(-1), (N,)).copy()
+    ge = np.broadcast_to(np.asarray(g_entropy, dtype=np.float64).reshape(-1), (N,)).copy()
+    if reduction == "mean":
+        n_valid = int(valid.sum())
+        s = 1.0 / n_valid if n_valid > 0 else 0.0
+        gl *= s
+        ge *= s
+    gl[~valid] = 0.0
+    ge[~valid] = 0.0
+    return gl, ge
+
+
+def dlogits_chunk(hidden, weight, labels, lse, ez, gl, ge, v0, v1,
+                  zloss_coef=0.0, softcap=0.0):
+    """Gradient of the objective w.r.t. the raw (pre-cap) logits z'[:, v0:v1]."""
+    z = logits_chunk(hidden, weight, v0, v1, softcap)
+    p = np.exp(z - lse[:, None])
+    onehot = (labels[:, None] == np.arange(v0, v1)[None, :]).astype(np.float64)
+    dz = gl[:, None] * (p - onehot + 2.0 * zloss_coef * lse[:, None] * p) \
+        - ge[:, None] * p * (z - ez[:, None])
+    if softcap != 0.0:
+        dz = dz * (1.0 - (z / softcap) ** 2)
+    return dz
+
+
+def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
+             ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, v_chunk=8192,
+             rows=None):
+    """(dhidden, dweight) in fp64.
+
+    ``lse``/``ez`` must come from :func:`forward` on the same inputs.  With
+    ``rows`` given, only dhidden[rows] is formed (dweight is then None): each
+    dhidden row needs only its own row of the logits.
+    """
+    hidden = np.asarray(hidden, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
+    gl, ge = grad_scales(g_loss, g_entropy, valid, reduction)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        hs, ls, vs = hidden[rows], lab[rows], valid[rows]
+        dh = np.zeros((rows.size, H))
+        for v0 in range(0, V, v_chunk):
+            v1 = min(V, v0 + v_chunk)
+            dz = dlogits_chunk(hs, weight, ls, lse[rows], ez[rows], gl[rows], ge[rows], v0, v1,
+                               zloss_coef, softcap)
+            dh += dz @ weight[:, v0:v1].T
+        return dh, None
+    dh = np.zeros((N, H))
+    dw = np.zeros((H, V))
+    for v0 in range(0, V, v_chunk):
+        v1 = min(V, v0 + v_chunk)
+        dz = dlogits_chunk(hidden, weight, lab, lse, ez, gl, ge, v0, v1, zloss_coef, softcap)
+        dh += dz @ weight[:, v0:v1].T
+        dw[:, v0:v1] = hidden.T @ dz
+    return dh, dw
+
+
+def objective(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
+              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0):
+    """J = <g_loss, loss> + <g_entropy, entropy> (scalar), the function whose gradient
+    :func:`backward` returns.  Used for finite-difference pins."""
+    out = forward(hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap)
+    gl = np.asarray(g_loss, dtype=np.float64).reshape(-1)
+    ge = np.asarray(g_entropy, dtype=np.float64).reshape(-1)
+    if reduction == "none":
+        return float(np.dot(gl * np.ones_like(out["loss"]), out["loss"])
+                     + np.dot(ge * np.ones_like(out["entropy"]), out["entropy"]))
+    return float(gl[0] * out["loss"] + ge[0] * out["entropy"])
