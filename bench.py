@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of fused linear cross-entropy + entropy (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = flce_forward + flce_backward over one batch of the workload (every
+kernel of the path).  Default workload: the Llama-3-8B LM-head shape
+(N=8192 tokens, H=4096, V=128256, 20 % ignored, z-loss 1e-4, mean).  Inputs are
+seeded synthetic tensors, resident in HBM before the timed region; the weight
+(about 1 GB) is larger than L2, so every pass streams it from HBM.
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) each rank runs an
+independent replica on its own GPU; value = all ranks' tokens / max rank time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead (the
+baseline arm), on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd tokens/sec and TFLOP/s (% of GB300 BF16 dense peak) at N×H×V"
+UNIT = "tokens/s"
+FALLBACK_BF16_TFLOPS = 1900.0  # profiling recipe fallback (burst), used only without a peaks file
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_head")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def workload_config(w, world):
+    return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "reduction": w.reduction,
+            "zloss_coef": w.zloss_coef, "softcap": w.softcap, "ignore_frac": w.ignore_frac,
+            "label_mode": w.label_mode, "grad_mode": w.grad_mode, "global_batch": w.N * world,
+            "seq_len": w.N, "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2: weight %.2f GB streamed from HBM every pass"
+                  % (w.H * w.V * 2 / 1e9)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample_step(w, h64, W64, labels_np, gl_np, ge_np, rows):
+    """fwd + bwd of the fp64 oracle on a row sample (dhidden of those rows and their
+    dweight contribution), as the oracle stands."""
+    from oracle import flce_oracle as orc
+    hs = h64[:rows]
+    ys = labels_np[:rows]
+    if w.reduction == "none":
+        gl, ge = gl_np[:rows], ge_np[:rows]
+    else:
+        gl, ge = gl_np, ge_np
+    o = orc.forward(hs, W64, ys, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap)
+    orc.backward(hs, W64, ys, o["lse"], o["ez"], gl, ge, w.reduction,
+                 zloss_coef=w.zloss_coef, softcap=w.softcap)
+    return o
+
+
+def oracle_inputs(w, hidden, weight, labels, g_loss, g_ent):
+    from linear_cross_entropy_forward_gb300.workloads import bf16_bits
+    from oracle import flce_oracle as orc
+    h64 = orc.bf16_bits_to_f64(bf16_bits(hidden))
+    W64 = orc.bf16_bits_to_f64(bf16_bits(weight))
+    return h64, W64, labels.numpy(), g_loss.numpy(), g_ent.numpy()
+
+
+def calibrate_rows(w, args_oracle, seconds):
+    """Rows per oracle sample so that one sample takes about `seconds`."""
+    r0 = 8
+    t0 = time.perf_counter()
+    oracle_sample_step(w, *args_oracle, rows=r0)
+    t = max(time.perf_counter() - t0, 1e-3)
+    return max(1, min(w.N, int(r0 * seconds / t))), t
+
+
+def cpu_baseline(w, hidden, weight, labels, g_loss, g_ent, seconds):
+    ai = oracle_inputs(w, hidden, weight, labels, g_loss, g_ent)
+    rows, _ = calibrate_rows(w, ai, seconds)
+    t0 = time.perf_counter()
+    oracle_sample_step(w, *ai, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle fwd+bwd on the first {rows} of {w.N} rows "
+                      f"(full H={w.H}, V={w.V}), {dt:.1f} s; BLAS threads = host cores"}
+
+
+# ---------------------------------------------------------------- clocks sampler
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not rows:
+            rows = [s for (_, s) in self.samples[-3:]]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w": statistics.median(power), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def nvsmi_id(torch, dev_index):
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[dev_index]
+        return str(dev_index)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("bf16_tflops_sustained", "bf16_tflops"):
+                if key in d and d[key]:
+                    return float(d[key]), f"of measured ({key})"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "of fallback (1.9 PFLOP/s bf16 burst)"
+
+
+def load_traffic(workload):
+    """Per-launch DRAM bytes of the forward GEMM from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+        return d.get(workload, {}).get("fwd_stats_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward, kernel_launches,
+                                                    make_params, workspace_size)
+    from linear_cross_entropy_forward_gb300.build import build
+    from linear_cross_entropy_forward_gb300.workloads import WORKLOADS, make_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0 or world == 1:
+        build()
+    if pg:
+        pg.barrier()
+    build()  # no-op once built; loads nothing yet
+
+    w = WORKLOADS[args.workload]
+    label_dev = "cuda" if w.label_mode == "self" else "cpu"
+    hidden, weight, labels, g_loss, g_ent = make_inputs(w, label_device=label_dev)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    gld, ged = g_loss.to(dev), g_ent.to(dev)
+    N, H, V = w.N, w.H, w.V
+    n_out = N if w.reduction == "none" else 1
+    loss = torch.empty(n_out, device=dev)
+    ent = torch.empty(n_out, device=dev)
+    lse = torch.empty(N, device=dev)
+    ez = torch.empty(N, device=dev)
+    dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(H, V, dtype=torch.bfloat16, device=dev)
+    p = make_params(N, H, V, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap)
+    ws_f = torch.empty(workspace_size(p, 0), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(workspace_size(p, 1), dtype=torch.uint8, device=dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+
+    def fwd():
+        flce_forward(hd, Wd, yd, w.reduction, workspace=ws_f, out=(loss, ent, lse, ez), **kw)
+
+    def bwd():
+        flce_backward(hd, Wd, yd, lse, ez, gld, ged, w.reduction, workspace=ws_b, out=(dh, dw),
+                      **kw)
+
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    sampler = ClockSampler(nvsmi_id(torch, local))
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_host0 = time.time()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    total_ms = e_start.elapsed_time(e_end)
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+        pg.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    peak_extra = torch.cuda.max_memory_allocated(dev) - mem0
+
+    # end to end: pinned host inputs -> device, fwd + bwd, loss/entropy back to host
+    hp = hidden.pin_memory()
+    Wp = weight.pin_memory()
+    yp = labels.pin_memory()
+    glp, gep = g_loss.pin_memory(), g_ent.pin_memory()
+    loss_h = torch.empty(n_out).pin_memory()
+    ent_h = torch.empty(n_out).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hp, Wp, yp, glp, gep))
+    d2h = 2 * n_out * 4
+
+    def e2e_step():
+        hd.copy_(hp, non_blocking=True)
+        Wd.copy_(Wp, non_blocking=True)
+        yd.copy_(yp, non_blocking=True)
+        gld.copy_(glp, non_blocking=True)
+        ged.copy_(gep, non_blocking=True)
+        fwd()
+        bwd()
+        loss_h.copy_(loss, non_blocking=True)
+        ent_h.copy_(ent, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    ms_step = total_ms / K
+    tokens = N * world
+    value = tokens / (ms_step / 1e3)
+    flops_step = 8.0 * N * H * V
+    tflops = flops_step / (ms_step / 1e3) / 1e12
+    peak, peak_src = load_peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_tflops = 2.0 * N * H * V / (fwd_avg / 1e3) / 1e12
+    bwd_tflops = 6.0 * N * H * V / (bwd_avg / 1e3) / 1e12
+    launches = (kernel_launches(p, 0) + kernel_launches(p, 1)) * K
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, world),
+        "tflops": tflops * world, "pct_peak": 100.0 * tflops / peak,
+        "peak_tflops": peak, "peak_source": peak_src,
+        "fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "roofline": {"bound": "tensor", "kernel": "flce_gemm_kernel<fwd_stats> (flce_forward)",
+                     "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": fwd_tflops / peak, "peak_note": peak_src,
+                     "algorithmic": "2*N*H*V flops per launch",
+                     "traffic": load_traffic(w.name)},
+        "roofline_step": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                          "unit": "TFLOP/s", "frac": tflops / peak,
+                          "algorithmic": "8*N*H*V flops per step (fwd 2, bwd 6 incl. recompute)"},
+        "memory": {"peak_extra_bytes": int(peak_extra),
+                   "workspace_fwd_bytes": int(ws_f.numel()),
+                   "workspace_bwd_bytes": int(ws_b.numel()),
+                   "unfused_fp32_logits_bytes": int(N * V * 4)},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
+                                           args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from linear_cross_entropy_forward_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    if w.label_mode == "self":
+        import torch
+        label_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    else:
+        label_dev = "cpu"
+    hidden, weight, labels, g_loss, g_ent = make_inputs(w, label_device=label_dev)
+    ai = oracle_inputs(w, hidden, weight, labels, g_loss, g_ent)
+    per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    rows, _ = calibrate_rows(w, ai, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, *ai, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(w, *ai, rows=rows)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = rows / dt
+    sample = (f"fp64 numpy oracle fwd+bwd on the first {rows} of {w.N} rows per step "
+              f"(full H={w.H}, V={w.V})")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(w, 1),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,130 @@
+/*
+ * flce.h -- C ABI of the fused linear cross-entropy + entropy library (libflce.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (verl PR #462, "Equivalent compute logic" and "API"):
+ *     logits  = hidden[N,H] @ weight[H,V]                (never stored)
+ *     z       = softcap * tanh(logits / softcap)          (softcap > 0 only;
+ *                                                          Liger-Kernel issue #127)
+ *     p       = softmax(z) over the vocabulary
+ *     lse_n   = logsumexp_v z_nv,   Ez_n = sum_v p_nv z_nv
+ *     ce_n    = lse_n - z_{n,y_n}                         (the page returns -ce as logprobs)
+ *     ent_n   = lse_n - Ez_n                              (entropy of p_n)
+ *     loss_n  = ce_n + zloss_coef * lse_n^2               (z-loss: Liger-Kernel PR #435,
+ *                                                          "Changes Made"; formula is a reading)
+ *   Rows whose label equals ignore_index contribute exactly 0 to loss and entropy
+ *   (Liger-Kernel PR #551, review: mean divides by the non-ignored count).
+ *   Reduction (Liger-Kernel PR #435, "Summary"): NONE returns loss[N], entropy[N];
+ *   SUM returns the sums over non-ignored rows; MEAN divides both sums by the
+ *   number of non-ignored rows (0 when every row is ignored).
+ *
+ *   Backward, for upstream gradients g_loss, g_entropy (per token for NONE,
+ *   scalars otherwise; scaled by 1/n_valid for MEAN; zero on ignored rows):
+ *     dz_nv   = gl_n (p_nv - [v == y_n] + 2 coef lse_n p_nv) - ge_n p_nv (z_nv - Ez_n)
+ *     dz'_nv  = dz_nv (1 - (z_nv/softcap)^2)              (soft-cap chain rule)
+ *     dhidden = dz' @ weight^T,   dweight = hidden^T @ dz'
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers to dense row-major arrays, owned by
+ *     the caller; the library allocates no device memory and keeps no state
+ *     between calls apart from a per-device cache of kernel attributes.
+ *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns).
+ *     labels: int64.  Everything else: fp32.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued asynchronously on it; nothing synchronises unless params->validate
+ *     is set.
+ *   - Return value: FLCE_OK or one of the FLCE_ERR_* codes below.  Argument errors
+ *     are detected on the host before anything is enqueued.  Device-side
+ *     conditions (a label outside [0,V) that is not ignore_index, a pipeline wait
+ *     that timed out) are recorded in an error word inside the workspace; they
+ *     are returned by flce_status(), or directly when params->validate != 0.
+ *   - Requirements: N >= 0, H >= 8, V >= 1, H % 8 == 0, V % 8 == 0 (16-byte row
+ *     strides for the TMA engine); every pointer 16-byte aligned.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLCE_RED_NONE = 0,
+  FLCE_RED_MEAN = 1,
+  FLCE_RED_SUM = 2
+} flce_reduction;
+
+enum {
+  FLCE_OK = 0,
+  FLCE_ERR_BAD_ARG = 1,       /* NULL pointer, bad reduction, negative coefficient */
+  FLCE_ERR_BAD_SHAPE = 2,     /* N, H or V out of the supported range */
+  FLCE_ERR_ALIGN = 3,         /* H or V not a multiple of 8, or a pointer not 16-byte aligned */
+  FLCE_ERR_WS_TOO_SMALL = 4,  /* ws_bytes < flce_workspace_size(...) */
+  FLCE_ERR_LABEL = 5,         /* a label outside [0, V) that is not ignore_index */
+  FLCE_ERR_TIMEOUT = 6,       /* a device pipeline wait exceeded its time limit */
+  FLCE_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed */
+  FLCE_ERR_DEVICE = 8         /* current device is not an sm_103 GPU */
+};
+
+typedef struct {
+  int64_t N;             /* tokens (rows of hidden) */
+  int64_t H;             /* hidden size */
+  int64_t V;             /* vocabulary size */
+  int64_t ignore_index;  /* label value that marks an ignored row (usually -100) */
+  int32_t reduction;     /* flce_reduction */
+  float zloss_coef;      /* z-loss coefficient, 0 = off */
+  float softcap;         /* tanh logit soft-cap c, 0 = off */
+  int32_t validate;      /* != 0: synchronise at the end and report device errors */
+  int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto */
+} flce_params;
+
+/* Bytes of device workspace that flce_forward (phase 0) or flce_backward (phase 1)
+ * needs for these parameters; 0 when the parameters are invalid.  The workspace is
+ * scratch: its contents need not be preserved between calls. */
+size_t flce_workspace_size(const flce_params* params, int phase);
+
+/* Forward pass.
+ *   hidden  [N,H] bf16, weight [H,V] bf16, labels [N] int64.
+ *   loss, entropy: [N] fp32 for FLCE_RED_NONE, [1] fp32 otherwise (overwritten).
+ *   lse, ez: [N] fp32, per-row logsumexp and softmax mean E_p[z] of the capped
+ *     logits, written for every row (ignored ones too); flce_backward needs them.
+ *   workspace: >= flce_workspace_size(params, 0) bytes, 256-byte aligned. */
+int flce_forward(const flce_params* params, const void* hidden, const void* weight,
+                 const int64_t* labels, float* loss, float* entropy, float* lse, float* ez,
+                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward pass (logits are recomputed tile by tile; no [N,V] array exists).
+ *   hidden, weight, labels: as given to flce_forward.
+ *   lse, ez: the [N] outputs of flce_forward for the same inputs and params.
+ *   g_loss, g_entropy: upstream gradients of loss and entropy, [N] for
+ *     FLCE_RED_NONE, [1] otherwise; NULL means zero.
+ *   dhidden [N,H] bf16, dweight [H,V] bf16: overwritten.
+ *   workspace: >= flce_workspace_size(params, 1) bytes, 256-byte aligned. */
+int flce_backward(const flce_params* params, const void* hidden, const void* weight,
+                  const int64_t* labels, const float* lse, const float* ez,
+                  const float* g_loss, const float* g_entropy, void* dhidden, void* dweight,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream` and returns the device-side status recorded in the
+ * workspace header by the last call that used this workspace (FLCE_OK,
+ * FLCE_ERR_LABEL or FLCE_ERR_TIMEOUT), or FLCE_ERR_CUDA. */
+int flce_status(const void* workspace, void* stream);
+
+/* Number of kernels one flce_forward (phase 0) or flce_backward (phase 1) call
+ * with these parameters enqueues (memsets not counted); -1 when invalid. */
+int flce_kernel_launches(const flce_params* params, int phase);
+
+/* Static, NUL-terminated description of a status code. */
+const char* flce_strerror(int code);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int flce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

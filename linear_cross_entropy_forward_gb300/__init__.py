@@ -1,0 +1,15 @@
+"""Fused linear cross-entropy + entropy for NVIDIA GB300 (sm_103a).
+
+loss, entropy = linear_cross_entropy(hidden, weight, labels, reduction="mean")
+
+The [N, V] logits are never materialised: tcgen05 tensor-core GEMM tiles feed
+fused online-softmax (forward) and dlogits (backward) epilogues inside
+libflce.so, reached through a C ABI (include/flce.h).
+"""
+from ._binding import (FlceError, FlceParams, flce_backward, flce_forward,  # noqa: F401
+                       flce_status, kernel_launches, linear_cross_entropy, load_library,
+                       make_params,
+                       workspace_size, LIB_PATH, EXPORTED)
+from .workloads import IGNORE_INDEX, WORKLOADS  # noqa: F401
+
+__version__ = "0.1.0"

@@ -1,0 +1,234 @@
+"""ctypes binding of libflce.so (include/flce.h).
+
+Argument marshalling only: tensors become raw device pointers plus sizes and
+the current CUDA stream; every step of the computation runs in the library's
+kernels.  If the library has not been built, or the device is not a GB300
+(sm_103), the calls raise -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .workloads import IGNORE_INDEX, RED_MEAN, RED_NONE, RED_SUM, reduction_code
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libflce.so")
+
+FLCE_OK = 0
+_ERR_NAMES = {1: "BAD_ARG", 2: "BAD_SHAPE", 3: "ALIGN", 4: "WS_TOO_SMALL", 5: "LABEL",
+              6: "TIMEOUT", 7: "CUDA", 8: "DEVICE"}
+
+
+class FlceError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"flce error {code} ({_ERR_NAMES.get(code, '?')}): {msg}")
+        self.code = code
+
+
+class FlceParams(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("H", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("ignore_index", ctypes.c_int64), ("reduction", ctypes.c_int32),
+                ("zloss_coef", ctypes.c_float), ("softcap", ctypes.c_float),
+                ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
+            "flce_kernel_launches", "flce_strerror", "flce_version")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libflce.so (once) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m linear_cross_entropy_forward_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(FlceParams)
+        vp = ctypes.c_void_p
+        lib.flce_workspace_size.argtypes = [P, ctypes.c_int]
+        lib.flce_workspace_size.restype = ctypes.c_size_t
+        lib.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.flce_forward.restype = ctypes.c_int
+        lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                      vp]
+        lib.flce_backward.restype = ctypes.c_int
+        lib.flce_status.argtypes = [vp, vp]
+        lib.flce_status.restype = ctypes.c_int
+        lib.flce_strerror.argtypes = [ctypes.c_int]
+        lib.flce_strerror.restype = ctypes.c_char_p
+        lib.flce_kernel_launches.argtypes = [P, ctypes.c_int]
+        lib.flce_kernel_launches.restype = ctypes.c_int
+        lib.flce_version.argtypes = []
+        lib.flce_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(code: int):
+    if code != FLCE_OK:
+        raise FlceError(code, load_library().flce_strerror(code).decode())
+
+
+def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
+                softcap=0.0, validate=False, chunk_v=0) -> FlceParams:
+    return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
+                      float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v))
+
+
+def workspace_size(params: FlceParams, phase: int) -> int:
+    n = load_library().flce_workspace_size(ctypes.byref(params), phase)
+    if n == 0:
+        raise FlceError(1, "invalid parameters for workspace sizing")
+    return int(n)
+
+
+def kernel_launches(params: FlceParams, phase: int) -> int:
+    """Kernels one forward (phase 0) / backward (phase 1) call enqueues."""
+    return int(load_library().flce_kernel_launches(ctypes.byref(params), phase))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(params, phase, device, workspace):
+    need = workspace_size(params, phase)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
+                 zloss_coef=0.0, softcap=0.0, validate=False, workspace=None, stream=None,
+                 out=None):
+    """Forward pass through the C ABI.
+
+    Returns (loss, entropy, lse, ez): loss/entropy are [N] for reduction 'none'
+    and [1] otherwise; lse/ez are the per-row [N] statistics saved for backward.
+    """
+    lib = load_library()
+    N, H = hidden.shape
+    V = weight.shape[1]
+    _need(hidden, "hidden", torch.bfloat16, (N, H))
+    _need(weight, "weight", torch.bfloat16, (H, V))
+    _need(labels, "labels", torch.int64, (N,))
+    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate)
+    dev = hidden.device
+    n_out = N if p.reduction == RED_NONE else 1
+    if out is None:
+        loss = torch.empty(n_out, dtype=torch.float32, device=dev)
+        ent = torch.empty(n_out, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        ez = torch.empty(N, dtype=torch.float32, device=dev)
+    else:
+        loss, ent, lse, ez = out
+    ws = _workspace(p, 0, dev, workspace)
+    _check(lib.flce_forward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
+                            _ptr(loss), _ptr(ent), _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
+                            _stream(stream)))
+    return loss, ent, lse, ez
+
+
+def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
+                  ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, validate=False,
+                  chunk_v=0, workspace=None, stream=None, out=None):
+    """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight [H,V] bf16).
+
+    g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
+    """
+    lib = load_library()
+    N, H = hidden.shape
+    V = weight.shape[1]
+    _need(hidden, "hidden", torch.bfloat16, (N, H))
+    _need(weight, "weight", torch.bfloat16, (H, V))
+    _need(labels, "labels", torch.int64, (N,))
+    _need(lse, "lse", torch.float32, (N,))
+    _need(ez, "ez", torch.float32, (N,))
+    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v)
+    n_g = N if p.reduction == RED_NONE else 1
+    if g_loss is not None:
+        _need(g_loss, "g_loss", torch.float32, (n_g,))
+    if g_entropy is not None:
+        _need(g_entropy, "g_entropy", torch.float32, (n_g,))
+    dev = hidden.device
+    if out is None:
+        dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(H, V, dtype=torch.bfloat16, device=dev)
+    else:
+        dh, dw = out
+    ws = _workspace(p, 1, dev, workspace)
+    _check(lib.flce_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
+                             _ptr(lse), _ptr(ez), _ptr(g_loss), _ptr(g_entropy), _ptr(dh),
+                             _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)))
+    return dh, dw
+
+
+def flce_status(workspace, stream=None) -> int:
+    """Device-side status of the last call that used `workspace` (synchronises)."""
+    return int(load_library().flce_status(_ptr(workspace), _stream(stream)))
+
+
+class _LinearCrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap):
+        loss, ent, lse, ez = flce_forward(hidden, weight, labels, reduction, ignore_index,
+                                          zloss_coef, softcap)
+        ctx.save_for_backward(hidden, weight, labels, lse, ez)
+        ctx.cfg = (reduction, ignore_index, zloss_coef, softcap)
+        if reduction_code(reduction) != RED_NONE:
+            loss, ent = loss[0], ent[0]
+        return loss, ent
+
+    @staticmethod
+    def backward(ctx, g_loss, g_ent):
+        hidden, weight, labels, lse, ez = ctx.saved_tensors
+        reduction, ignore_index, zloss_coef, softcap = ctx.cfg
+        n_g = hidden.shape[0] if reduction_code(reduction) == RED_NONE else 1
+
+        def prep(g):
+            if g is None:
+                return None
+            return g.detach().reshape(n_g).to(torch.float32).contiguous()
+
+        dh, dw = flce_backward(hidden, weight, labels, lse, ez, prep(g_loss), prep(g_ent),
+                               reduction, ignore_index, zloss_coef, softcap)
+        return dh, dw, None, None, None, None, None
+
+
+def linear_cross_entropy(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
+                         zloss_coef=0.0, softcap=0.0):
+    """loss, entropy = linear_cross_entropy(hidden, weight, labels, reduction)
+
+    The call of verl PR #462 ("API"): hidden [N,H] bf16, weight [H,V] bf16,
+    labels [N] int64.  `loss` is the cross-entropy (+ z-loss); the page's
+    log-probability is -loss when z-loss is off.  Differentiable w.r.t. hidden
+    and weight.
+    """
+    return _LinearCrossEntropy.apply(hidden, weight, labels, reduction, ignore_index,
+                                     zloss_coef, softcap)

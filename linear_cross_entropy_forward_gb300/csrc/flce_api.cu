@@ -1,0 +1,548 @@
+// C ABI of libflce.so: argument checks, workspace layout, TMA descriptors and
+// the launch sequence of the forward and backward passes (declared in flce.h).
+//
+// Forward  (verl PR #462, "Equivalent compute logic", without the [N,V] logits):
+//   1. fwd_stats GEMM: hidden @ weight tile by tile, each 128-column block of a
+//      row reduced to online-softmax partials (m, d, s) plus the label logit.
+//   2. fwd_combine: merge the partials of a row -> lse, E_p[z], CE, entropy,
+//      z-loss, ignore mask (Liger-Kernel PR #551 / PR #435 semantics).
+//   3. reduce (mean/sum only): fixed-order fp64 sum over rows.
+// Backward, per vocabulary chunk of width Vc (after a per-row prep kernel):
+//   4. bwd_dlogits GEMM: recompute logits, write dlogits[N, Vc] (bf16).
+//   5. bwd_dweight GEMM: dweight[:, chunk] = hidden^T @ dlogits.
+//   6. bwd_dhidden GEMM: dhidden (fp32 accumulator) += dlogits @ weight[:, chunk]^T;
+//      the last chunk writes bf16.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/flce.h"
+#include "flce_gemm.cuh"
+
+namespace flce {
+
+cudaError_t launch_fwd_stats(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
+                             const EpiArgs&, int, cudaStream_t);
+cudaError_t launch_bwd_dlogits(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
+                               const EpiArgs&, int, cudaStream_t);
+cudaError_t launch_bwd_dweight(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
+                               const EpiArgs&, int, cudaStream_t);
+cudaError_t launch_bwd_dhidden(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
+                               const EpiArgs&, int, cudaStream_t);
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr size_t kHeaderBytes = 256;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kDefaultChunkBytes = int64_t(256) << 20;  // dlogits chunk target
+
+// Descriptor strides of the MN-major operand tiles: 64-wide MN atoms 8 KB apart
+// (leading byte offset), 8-row K groups 1 KB apart (stride byte offset).
+constexpr uint32_t kMnLbo = MN_ATOM_BYTES;
+constexpr uint32_t kMnSbo = 1024;
+
+// ------------------------------------------------------------ small kernels
+__device__ __forceinline__ void merge_stats(float& M, float& D, float& S, float m, float d,
+                                            float s) {
+  const float Mn = fmaxf(M, m);
+  const float a1 = exp2f(M - Mn);
+  const float a2 = exp2f(m - Mn);
+  S = a1 * fmaf(M - Mn, D, S) + a2 * fmaf(m - Mn, d, s);
+  D = a1 * D + a2 * d;
+  M = Mn;
+}
+
+// One block of 8 warps handles 32 rows; warp w merges parts w, w+8, ...
+__global__ void __launch_bounds__(256) fwd_combine_kernel(
+    const float* __restrict__ pm, const float* __restrict__ pd, const float* __restrict__ ps,
+    int64_t n_parts, int64_t N, const float* __restrict__ zlabel,
+    const int64_t* __restrict__ labels, int64_t V, int64_t ignore_index, float zcoef,
+    float* __restrict__ lse_out, float* __restrict__ ez_out, float* __restrict__ loss_row,
+    float* __restrict__ ent_row, uint32_t* err) {
+  __shared__ float sM[8][32], sD[8][32], sS[8][32];
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  float M = -1e30f, D = 0.0f, S = 0.0f;
+  if (n < N) {
+    for (int64_t p = w; p < n_parts; p += 8) {
+      const int64_t o = p * N + n;
+      merge_stats(M, D, S, pm[o], pd[o], ps[o]);
+    }
+  }
+  sM[w][lane] = M;
+  sD[w][lane] = D;
+  sS[w][lane] = S;
+  __syncthreads();
+  if (w != 0 || n >= N) return;
+  M = sM[0][lane];
+  D = sD[0][lane];
+  S = sS[0][lane];
+  for (int k = 1; k < 8; ++k) merge_stats(M, D, S, sM[k][lane], sD[k][lane], sS[k][lane]);
+  // M, S in log2 units: lse = ln2 (M + log2 D); entropy = ln d - s_c/d = ln2 (log2 D - S/D)
+  const float l2d = log2f(D);
+  const float lse = kLn2 * (M + l2d);
+  const float ent = kLn2 * (l2d - S / D);
+  lse_out[n] = lse;
+  ez_out[n] = lse - ent;
+  const int64_t y = labels[n];
+  float lt = 0.0f, et = 0.0f;
+  if (y != ignore_index) {
+    if (y < 0 || y >= V) {
+      atomicOr(err, FLCE_DEVERR_LABEL);
+      lt = et = __int_as_float(0x7fc00000);
+    } else {
+      lt = (lse - zlabel[n]) + zcoef * lse * lse;
+      et = ent;
+    }
+  }
+  loss_row[n] = lt;
+  ent_row[n] = et;
+}
+
+// Deterministic fixed-order reduction over rows (one block): mean or sum.
+__global__ void __launch_bounds__(1024) reduce_rows_kernel(
+    const float* __restrict__ loss_row, const float* __restrict__ ent_row,
+    const int64_t* __restrict__ labels, int64_t N, int64_t ignore_index, int mean,
+    float* __restrict__ loss_out, float* __restrict__ ent_out) {
+  __shared__ double sl[1024], se[1024];
+  __shared__ long long sc[1024];
+  double l = 0.0, e = 0.0;
+  long long c = 0;
+  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+    l += loss_row[n];
+    e += ent_row[n];
+    c += labels[n] != ignore_index;
+  }
+  sl[threadIdx.x] = l;
+  se[threadIdx.x] = e;
+  sc[threadIdx.x] = c;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) {
+      sl[threadIdx.x] += sl[threadIdx.x + s];
+      se[threadIdx.x] += se[threadIdx.x + s];
+      sc[threadIdx.x] += sc[threadIdx.x + s];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double L = sl[0], E = se[0];
+    if (mean) {
+      const long long nv = sc[0];
+      L = nv > 0 ? L / static_cast<double>(nv) : 0.0;
+      E = nv > 0 ? E / static_cast<double>(nv) : 0.0;
+    }
+    loss_out[0] = static_cast<float>(L);
+    ent_out[0] = static_cast<float>(E);
+  }
+}
+
+// Per-row constants of the dlogits epilogue:
+// (lse*log2e, a (1 + 2 coef lse) + b Ez, b, a), a/b the scaled upstream grads.
+__global__ void __launch_bounds__(1024) bwd_prep_kernel(
+    const int64_t* __restrict__ labels, const float* __restrict__ lse,
+    const float* __restrict__ ez, const float* __restrict__ g_loss,
+    const float* __restrict__ g_ent, int64_t N, int64_t ignore_index, int per_token, int mean,
+    float zcoef, float4* __restrict__ rowc) {
+  __shared__ long long sc[1024];
+  long long c = 0;
+  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) c += labels[n] != ignore_index;
+  sc[threadIdx.x] = c;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) sc[threadIdx.x] += sc[threadIdx.x + s];
+    __syncthreads();
+  }
+  const long long nv = sc[0];
+  const float scale = mean ? (nv > 0 ? 1.0f / static_cast<float>(nv) : 0.0f) : 1.0f;
+  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+    const bool valid = labels[n] != ignore_index;
+    const int64_t gi = per_token ? n : 0;
+    const float gl = g_loss ? g_loss[gi] : 0.0f;
+    const float ge = g_ent ? g_ent[gi] : 0.0f;
+    const float a = valid ? gl * scale : 0.0f;
+    const float b = valid ? ge * scale : 0.0f;
+    const float l = lse[n];
+    rowc[n] = make_float4(l * kLog2e, fmaf(a, fmaf(2.0f * zcoef, l, 1.0f), b * ez[n]), b, a);
+  }
+}
+
+// ------------------------------------------------------------ host helpers
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct FwdLayout {
+  size_t pm, pd, ps, zlabel, loss_row, ent_row, total;
+  int64_t n_parts;
+};
+
+FwdLayout fwd_layout(const flce_params* p) {
+  FwdLayout L{};
+  L.n_parts = 2 * cdiv(p->V, BN);
+  const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * p->N) * 4);
+  const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
+  size_t off = kHeaderBytes;
+  L.pm = off; off += part_bytes;
+  L.pd = off; off += part_bytes;
+  L.ps = off; off += part_bytes;
+  L.zlabel = off; off += row_bytes;
+  L.loss_row = off; off += row_bytes;
+  L.ent_row = off; off += row_bytes;
+  L.total = off;
+  return L;
+}
+
+struct BwdLayout {
+  size_t rowc, dl, acc, total;
+  int64_t Vc, chunks;
+};
+
+int64_t chunk_width(const flce_params* p) {
+  const int64_t vfull = cdiv(p->V, BN) * BN;
+  int64_t vc = p->chunk_v;
+  if (vc <= 0) {
+    const int64_t n = p->N > 0 ? p->N : 1;
+    vc = (kDefaultChunkBytes / (2 * n)) / BN * BN;
+  }
+  if (vc < BN) vc = BN;
+  if (vc > vfull) vc = vfull;
+  return vc;
+}
+
+BwdLayout bwd_layout(const flce_params* p) {
+  BwdLayout L{};
+  L.Vc = chunk_width(p);
+  L.chunks = cdiv(p->V, L.Vc);
+  size_t off = kHeaderBytes;
+  L.rowc = off; off += align256(static_cast<size_t>(p->N) * 16);
+  L.dl = off; off += align256(static_cast<size_t>(p->N) * L.Vc * 2);
+  L.acc = off;
+  if (L.chunks > 1) off += align256(static_cast<size_t>(p->N) * p->H * 4);
+  L.total = off;
+  return L;
+}
+
+int check_params(const flce_params* p) {
+  if (!p) return FLCE_ERR_BAD_ARG;
+  if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_SUM) return FLCE_ERR_BAD_ARG;
+  if (!(p->zloss_coef >= 0.0f) || !(p->softcap >= 0.0f)) return FLCE_ERR_BAD_ARG;
+  if (p->N < 0 || p->H < 8 || p->V < 1) return FLCE_ERR_BAD_SHAPE;
+  if (p->N > kMaxDim || p->H > kMaxDim || p->V > kMaxDim) return FLCE_ERR_BAD_SHAPE;
+  if (p->H % 8 != 0 || p->V % 8 != 0) return FLCE_ERR_ALIGN;
+  if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % BN != 0)) return FLCE_ERR_BAD_ARG;
+  // chunk-relative and vocabulary column indices are 32-bit inside the kernels
+  if (cdiv(p->V, BN) * BN > kMaxDim) return FLCE_ERR_BAD_SHAPE;
+  return FLCE_OK;
+}
+
+inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the library
+// links no libcuda at build time.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array with a {box_inner, box_outer}
+// box, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+              int64_t row_elems, int box_inner, int box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+int device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FLCE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (major != 10 || minor != 3) return FLCE_ERR_DEVICE;
+    cache[dev].sms = sms;
+    cache[dev].ok = true;
+  }
+  *out = cache[dev];
+  return FLCE_OK;
+}
+
+int read_status(const void* workspace, cudaStream_t st) {
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
+  if (word & FLCE_DEVERR_LABEL) return FLCE_ERR_LABEL;
+  return FLCE_OK;
+}
+
+inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
+
+GemmShape base_shape() {
+  GemmShape sh{};
+  sh.mn_lbo = kMnLbo;
+  sh.mn_sbo = kMnSbo;
+  return sh;
+}
+
+}  // namespace
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+int flce_version(void) { return kVersion; }
+
+const char* flce_strerror(int code) {
+  switch (code) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_BAD_ARG: return "invalid argument";
+    case FLCE_ERR_BAD_SHAPE: return "unsupported shape (need N >= 0, H >= 8, V >= 1)";
+    case FLCE_ERR_ALIGN: return "H and V must be multiples of 8 and pointers 16-byte aligned";
+    case FLCE_ERR_WS_TOO_SMALL: return "workspace smaller than flce_workspace_size()";
+    case FLCE_ERR_LABEL: return "label outside [0, V) that is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FLCE_ERR_CUDA: return "CUDA call failed";
+    case FLCE_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+size_t flce_workspace_size(const flce_params* p, int phase) {
+  if (check_params(p) != FLCE_OK) return 0;
+  if (phase == 0) return fwd_layout(p).total;
+  if (phase == 1) return bwd_layout(p).total;
+  return 0;
+}
+
+int flce_kernel_launches(const flce_params* p, int phase) {
+  if (check_params(p) != FLCE_OK || p->N == 0) return check_params(p) != FLCE_OK ? -1 : 0;
+  if (phase == 0) return p->reduction == FLCE_RED_NONE ? 2 : 3;
+  if (phase == 1) return 1 + 3 * static_cast<int>(bwd_layout(p).chunks);
+  return -1;
+}
+
+int flce_status(const void* workspace, void* stream) {
+  if (!workspace) return FLCE_ERR_BAD_ARG;
+  return read_status(workspace, static_cast<cudaStream_t>(stream));
+}
+
+int flce_forward(const flce_params* p, const void* hidden, const void* weight,
+                 const int64_t* labels, float* loss, float* entropy, float* lse, float* ez,
+                 void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!loss || !entropy || !workspace || !weight) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!hidden || !labels || !lse || !ez)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(loss) ||
+      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const FwdLayout L = fwd_layout(p);
+  if (ws_bytes < L.total) return FLCE_ERR_WS_TOO_SMALL;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  if ((rc = cuda_rc(cudaMemsetAsync(ws, 0, kHeaderBytes, st)))) return rc;
+  const bool per_token = p->reduction == FLCE_RED_NONE;
+  const int64_t N = p->N, H = p->H, V = p->V;
+
+  if (N == 0) {
+    if (!per_token) {
+      if ((rc = cuda_rc(cudaMemsetAsync(loss, 0, 4, st)))) return rc;
+      if ((rc = cuda_rc(cudaMemsetAsync(entropy, 0, 4, st)))) return rc;
+    }
+    return p->validate ? read_status(ws, st) : FLCE_OK;
+  }
+
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, hidden, H, N, H, BK, BM)) return FLCE_ERR_CUDA;
+  if (!make_map(&tmB, weight, V, H, V, 64, BK)) return FLCE_ERR_CUDA;
+  GemmShape sh = base_shape();
+  sh.m_tiles = static_cast<int>(cdiv(N, BM));
+  sh.n_tiles = static_cast<int>(cdiv(V, BN));
+  sh.k_blocks = static_cast<int>(cdiv(H, BK));
+  sh.raster = 0;
+  EpiArgs ea{};
+  ea.rows = static_cast<int>(N);
+  ea.cols = static_cast<int>(V);
+  ea.col_base = 0;
+  ea.V = V;
+  ea.softcap = p->softcap;
+  ea.labels = labels;
+  ea.ignore_index = p->ignore_index;
+  ea.pm = reinterpret_cast<float*>(ws + L.pm);
+  ea.pd = reinterpret_cast<float*>(ws + L.pd);
+  ea.ps = reinterpret_cast<float*>(ws + L.ps);
+  ea.part_stride = N;
+  ea.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
+  ea.err = err;
+  if ((rc = cuda_rc(launch_fwd_stats(tmA, tmB, sh, ea, di.sms, st)))) return rc;
+
+  float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
+  float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
+  fwd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 32)), 256, 0, st>>>(
+      ea.pm, ea.pd, ea.ps, L.n_parts, N, ea.zlabel, labels, V, p->ignore_index, p->zloss_coef,
+      lse, ez, loss_row, ent_row, err);
+  if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+  if (!per_token) {
+    reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,
+                                           p->reduction == FLCE_RED_MEAN, loss, entropy);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+  }
+  return p->validate ? read_status(ws, st) : FLCE_OK;
+}
+
+int flce_backward(const flce_params* p, const void* hidden, const void* weight,
+                  const int64_t* labels, const float* lse, const float* ez,
+                  const float* g_loss, const float* g_entropy, void* dhidden, void* dweight,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!weight || !dweight || !workspace) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!hidden || !labels || !lse || !ez || !dhidden)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(lse) ||
+      !aligned16(ez) || !aligned16(dhidden) || !aligned16(dweight) ||
+      (reinterpret_cast<uintptr_t>(g_loss) & 3) || (reinterpret_cast<uintptr_t>(g_entropy) & 3) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const BwdLayout L = bwd_layout(p);
+  if (ws_bytes < L.total) return FLCE_ERR_WS_TOO_SMALL;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  if ((rc = cuda_rc(cudaMemsetAsync(ws, 0, kHeaderBytes, st)))) return rc;
+  const int64_t N = p->N, H = p->H, V = p->V;
+
+  if (N == 0) {
+    // no rows: dweight = 0 (dhidden has no elements)
+    if ((rc = cuda_rc(cudaMemsetAsync(dweight, 0, static_cast<size_t>(H * V) * 2, st))))
+      return rc;
+    return p->validate ? read_status(ws, st) : FLCE_OK;
+  }
+
+  float4* rowc = reinterpret_cast<float4*>(ws + L.rowc);
+  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + L.dl);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  bwd_prep_kernel<<<1, 1024, 0, st>>>(labels, lse, ez, g_loss, g_entropy, N, p->ignore_index,
+                                      p->reduction == FLCE_RED_NONE,
+                                      p->reduction == FLCE_RED_MEAN, p->zloss_coef, rowc);
+  if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+
+  CUtensorMap mHidK, mWMn, mHidMn, mDlMn, mDlK, mWK;
+  bool ok = make_map(&mHidK, hidden, H, N, H, BK, BM) && make_map(&mWMn, weight, V, H, V, 64, BK) &&
+            make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
+            make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
+            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, BM) && make_map(&mWK, weight, V, H, V, BK, BN);
+  if (!ok) return FLCE_ERR_CUDA;
+
+  for (int64_t c = 0; c < L.chunks; ++c) {
+    const int64_t v0 = c * L.Vc;
+    const int64_t w = (V - v0) < L.Vc ? (V - v0) : L.Vc;
+    const int nt = static_cast<int>(cdiv(w, BN));
+
+    // dlogits[N, w] = f(hidden @ weight[:, v0:v0+w])
+    GemmShape s3 = base_shape();
+    s3.m_tiles = static_cast<int>(cdiv(N, BM));
+    s3.n_tiles = nt;
+    s3.k_blocks = static_cast<int>(cdiv(H, BK));
+    s3.raster = 0;
+    s3.b_mn_off = static_cast<int>(v0);
+    EpiArgs e3{};
+    e3.rows = static_cast<int>(N);
+    e3.cols = static_cast<int>(w);
+    e3.col_base = static_cast<int>(v0);
+    e3.V = V;
+    e3.softcap = p->softcap;
+    e3.labels = labels;
+    e3.ignore_index = p->ignore_index;
+    e3.rowc = rowc;
+    e3.dl = dl;
+    e3.ld_dl = L.Vc;
+    e3.err = err;
+    if ((rc = cuda_rc(launch_bwd_dlogits(mHidK, mWMn, s3, e3, di.sms, st)))) return rc;
+
+    // dweight[:, v0:v0+w] = hidden^T @ dlogits
+    GemmShape s4 = base_shape();
+    s4.m_tiles = static_cast<int>(cdiv(H, BM));
+    s4.n_tiles = nt;
+    s4.k_blocks = static_cast<int>(cdiv(N, BK));
+    s4.raster = 0;
+    EpiArgs e4{};
+    e4.rows = static_cast<int>(H);
+    e4.cols = static_cast<int>(w);
+    e4.col_base = static_cast<int>(v0);
+    e4.V = V;
+    e4.out = static_cast<__nv_bfloat16*>(dweight);
+    e4.ld_out = V;
+    e4.err = err;
+    if ((rc = cuda_rc(launch_bwd_dweight(mHidMn, mDlMn, s4, e4, di.sms, st)))) return rc;
+
+    // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
+    GemmShape s5 = base_shape();
+    s5.m_tiles = static_cast<int>(cdiv(N, BM));
+    s5.n_tiles = static_cast<int>(cdiv(H, BN));
+    s5.k_blocks = static_cast<int>(cdiv(w, BK));
+    s5.raster = 1;
+    s5.b_k_off = static_cast<int>(v0);
+    EpiArgs e5{};
+    e5.rows = static_cast<int>(N);
+    e5.cols = static_cast<int>(H);
+    e5.V = V;
+    e5.acc = acc;
+    e5.acc_out = static_cast<__nv_bfloat16*>(dhidden);
+    e5.ld_acc = H;
+    e5.acc_mode = L.chunks == 1 ? ACC_ONLY
+                  : c == 0      ? ACC_FIRST
+                  : c == L.chunks - 1 ? ACC_LAST
+                                      : ACC_MID;
+    e5.err = err;
+    if ((rc = cuda_rc(launch_bwd_dhidden(mDlK, mWK, s5, e5, di.sms, st)))) return rc;
+  }
+  return p->validate ? read_status(ws, st) : FLCE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,464 @@
+// Persistent, warp-specialised tcgen05 GEMM with fused epilogues for the fused
+// linear cross-entropy + entropy path (verl PR #462, "Equivalent compute logic":
+// logits = hidden @ weight are never stored; every use of them is fused here).
+//
+//   warp 0      TMA producer: bf16 tiles of A (BM x BK) and B (BN x BK) into a
+//               STAGES-deep ring of 128B-swizzled shared-memory buffers.
+//   warp 1      UMMA issuer: 128x256x16 tcgen05.mma into one of two 256-column
+//               fp32 TMEM accumulators (double buffered against the epilogue).
+//   warps 2..9  epilogue: tcgen05.ld one row per thread (warp w reads TMEM lanes
+//               32*(w%4)..+31, columns half (w-2)/4 of the tile), then one of:
+//     EPI_FWD_STATS  online-softmax partials per row and 128-column block:
+//                    running max m, sum-exp d and centred s = sum e^{u-m}(u-m)
+//                    in log2 units, plus the label logit (Liger-Kernel PR #551:
+//                    m and d of the online softmax feed the entropy).
+//     EPI_DLOGITS    recomputed logits -> dlogits (bf16) of the CE, z-loss and
+//                    entropy terms, with the soft-cap chain rule (Liger-Kernel
+//                    issue #127: tanh capping after the matmul).
+//     EPI_STORE_BF16 plain bf16 store (dweight tiles).
+//     EPI_ACCUM      fp32 split-V accumulation of dhidden; last chunk -> bf16.
+//
+// Operand majorness is a template choice: K-major tiles come in as one TMA box
+// {64, rows}; MN-major tiles as rows/64 boxes {64, 64} stacked 8 KB apart.
+#pragma once
+
+#include "flce_device.cuh"
+
+namespace flce {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int UK = 16;  // K of one kind::f16 UMMA
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;
+constexpr int B_TILE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // one {64 MN x 64 K} box
+
+enum EpiKind { EPI_FWD_STATS = 0, EPI_DLOGITS = 1, EPI_STORE_BF16 = 2, EPI_ACCUM = 3 };
+enum AccMode { ACC_FIRST = 0, ACC_MID = 1, ACC_LAST = 2, ACC_ONLY = 3 };
+
+struct GemmShape {
+  int m_tiles, n_tiles, k_blocks;
+  int raster;                 // 0: m fastest, 1: n fastest
+  int a_mn_off, a_k_off;      // added to A's (mn, k) tile coordinates
+  int b_mn_off, b_k_off;      // added to B's (mn, k) tile coordinates
+  uint32_t mn_lbo, mn_sbo;    // descriptor strides of MN-major operands (bytes)
+};
+
+struct EpiArgs {
+  int rows;            // valid output rows (M extent)
+  int cols;            // valid output columns, relative to the problem's column 0
+  int col_base;        // global column (vocab index) of problem column 0
+  int64_t V;           // vocabulary size (masking of the softmax)
+  float softcap;       // 0 = off
+  const int64_t* labels;
+  int64_t ignore_index;
+  // EPI_FWD_STATS
+  float* pm;
+  float* pd;
+  float* ps;
+  int64_t part_stride;  // elements between consecutive 128-column parts
+  float* zlabel;
+  // EPI_DLOGITS
+  const float4* rowc;   // per row: (lse*log2e, a(1+2 coef lse) + b Ez, b, a)
+  __nv_bfloat16* dl;
+  int64_t ld_dl;
+  // EPI_STORE_BF16
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  // EPI_ACCUM
+  float* acc;
+  __nv_bfloat16* acc_out;
+  int64_t ld_acc;
+  int acc_mode;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int& mt, int& nt) {
+  if (sh.raster == 0) {
+    mt = t % sh.m_tiles;
+    nt = t / sh.m_tiles;
+  } else {
+    nt = t % sh.n_tiles;
+    mt = t / sh.n_tiles;
+  }
+}
+
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                             int mn0, int k0) {
+  if constexpr (!MN) {
+    tma_load_2d(dst, map, bar, k0, mn0);
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j)
+      tma_load_2d(dst + j * MN_ATOM_BYTES, map, bar, mn0 + 64 * j, k0);
+  }
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, const GemmShape& sh) {
+  if constexpr (!MN) {
+    // K-major: the k-th 16-element slice starts 32 bytes further into each
+    // 128-byte swizzled row; 8-row groups are 1024 bytes apart.
+    return sdesc_sw128(base + kk * (UK * 2), 16, 1024);
+  } else {
+    // MN-major: 16 K-rows of 128 bytes per slice; 64-wide MN atoms 8 KB apart.
+    return sdesc_sw128(base + kk * (UK * 128), sh.mn_lbo, sh.mn_sbo);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+template <int EPI>
+struct Epilogue;
+
+// Online-softmax partial statistics of one row over 128 columns.
+template <>
+struct Epilogue<EPI_FWD_STATS> {
+  static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
+                                             int col0) {
+    const bool row_ok = row < ea.rows;
+    int y = -1;
+    if (row_ok) {
+      int64_t yl = ea.labels[row];
+      if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
+    }
+    const bool cap = ea.softcap != 0.0f;
+    const float inv_cap = cap ? 1.0f / ea.softcap : 0.0f;
+    const int vcol0 = ea.col_base + col0;
+    float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f;
+    bool hit = false;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float x[32];
+      tmem_ld32(tbase + c * 32, x);
+      const int vb = vcol0 + c * 32;
+      const int nvalid = static_cast<int>(ea.V - vb);
+      float cm = -1e30f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float z = x[j];
+        if (cap) z = ea.softcap * tanh_from_exp(z * inv_cap);
+        if (vb + j == y) {
+          zy = z;
+          hit = true;
+        }
+        float u = (j < nvalid) ? z * kLog2e : -1e30f;
+        x[j] = u;
+        cm = fmaxf(cm, u);
+      }
+      if (cm > mx) {
+        const float a = fast_ex2(mx - cm);
+        s = a * fmaf(mx - cm, d, s);
+        d *= a;
+        mx = cm;
+      }
+      if (nvalid >= 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float t = x[j] - mx;
+          const float e = fast_ex2(t);
+          d += e;
+          s = fmaf(e, t, s);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float t = x[j] - mx;
+          const float e = (j < nvalid) ? fast_ex2(t) : 0.0f;
+          d += e;
+          s = fmaf(e, t, s);
+        }
+      }
+    }
+    if (row_ok) {
+      const int64_t part = vcol0 / 128;
+      const int64_t o = part * ea.part_stride + row;
+      ea.pm[o] = mx;
+      ea.pd[o] = d;
+      ea.ps[o] = s;
+      if (hit) ea.zlabel[row] = zy;
+    }
+  }
+};
+
+// dlogits of one row over 128 columns of the current vocabulary chunk.
+template <>
+struct Epilogue<EPI_DLOGITS> {
+  static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
+                                             int col0) {
+    const bool row_ok = row < ea.rows;
+    float4 rc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int y = -1;
+    if (row_ok) {
+      rc = ea.rowc[row];
+      int64_t yl = ea.labels[row];
+      if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
+    }
+    const bool cap = ea.softcap != 0.0f;
+    const float inv_cap = cap ? 1.0f / ea.softcap : 0.0f;
+    const int vcol0 = ea.col_base + col0;
+    __nv_bfloat16* dst = ea.dl + static_cast<int64_t>(row) * ea.ld_dl + col0;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float x[32];
+      tmem_ld32(tbase + c * 32, x);
+      const int vb = vcol0 + c * 32;
+      const int nvalid = static_cast<int>(ea.V - vb);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float g2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float z = x[j + h];
+          float th = 0.0f;
+          if (cap) {
+            th = tanh_from_exp(z * inv_cap);
+            z = ea.softcap * th;
+          }
+          const float p = fast_ex2(fmaf(z, kLog2e, -rc.x));
+          float g = p * fmaf(-rc.z, z, rc.y);
+          if (vb + j + h == y) g -= rc.w;
+          if (cap) g *= fmaf(-th, th, 1.0f);
+          g2[h] = (j + h < nvalid) ? g : 0.0f;
+        }
+        pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+      }
+      if (row_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+};
+
+// bf16 store of a 128-column row segment (dweight).
+template <>
+struct Epilogue<EPI_STORE_BF16> {
+  static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
+                                             int col0) {
+    const bool row_ok = row < ea.rows;
+    __nv_bfloat16* dst = ea.out + static_cast<int64_t>(row) * ea.ld_out + ea.col_base + col0;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float x[32];
+      tmem_ld32(tbase + c * 32, x);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = col0 + c * 32 + q * 8;
+        if (col < ea.cols) {
+          uint4 v = make_uint4(pack_bf16x2(x[q * 8 + 0], x[q * 8 + 1]),
+                               pack_bf16x2(x[q * 8 + 2], x[q * 8 + 3]),
+                               pack_bf16x2(x[q * 8 + 4], x[q * 8 + 5]),
+                               pack_bf16x2(x[q * 8 + 6], x[q * 8 + 7]));
+          *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+        }
+      }
+    }
+  }
+};
+
+// fp32 accumulation across vocabulary chunks (dhidden).
+template <>
+struct Epilogue<EPI_ACCUM> {
+  static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
+                                             int col0) {
+    const bool row_ok = row < ea.rows;
+    const int64_t base = static_cast<int64_t>(row) * ea.ld_acc + col0;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float x[32];
+      tmem_ld32(tbase + c * 32, x);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = col0 + c * 32 + q * 8;
+        if (col >= ea.cols) continue;
+        float* a = ea.acc + base + c * 32 + q * 8;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = x[q * 8 + i];
+        if (ea.acc_mode == ACC_MID || ea.acc_mode == ACC_LAST) {
+          const float4 o0 = reinterpret_cast<const float4*>(a)[0];
+          const float4 o1 = reinterpret_cast<const float4*>(a)[1];
+          v[0] += o0.x; v[1] += o0.y; v[2] += o0.z; v[3] += o0.w;
+          v[4] += o1.x; v[5] += o1.y; v[6] += o1.z; v[7] += o1.w;
+        }
+        if (ea.acc_mode == ACC_FIRST || ea.acc_mode == ACC_MID) {
+          reinterpret_cast<float4*>(a)[0] = make_float4(v[0], v[1], v[2], v[3]);
+          reinterpret_cast<float4*>(a)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+          uint4 o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+          *reinterpret_cast<uint4*>(ea.acc_out + base + c * 32 + q * 8) = o;
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
+                     const EpiArgs ea) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int total = sh.m_tiles * sh.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, sh, mt, nt);
+        bool ok = true;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ea.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          const int k0 = kb * BK;
+          load_operand<A_MN, BM>(sA + stage * A_TILE_BYTES, &tmA, &full[stage],
+                                 mt * BM + sh.a_mn_off, k0 + sh.a_k_off);
+          load_operand<B_MN, BN>(sB + stage * B_TILE_BYTES, &tmB, &full[stage],
+                                 nt * BN + sh.b_mn_off, k0 + sh.b_k_off);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- UMMA issuer
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, ea.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, ea.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            umma_bf16(d_tmem, operand_desc<A_MN>(a_addr, kk, sh),
+                      operand_desc<B_MN>(b_addr, kk, sh), IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      int mt, nt;
+      tile_coords(t, sh, mt, nt);
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, ea.err)) break;
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + half * 128;
+      Epilogue<EPI>::run(ea, tbase, mt * BM + r, nt * BN + half * 128);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// Host-side launcher, instantiated in the gemm_*.cu translation units.
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh,
+                        const EpiArgs& ea, int num_sms, cudaStream_t stream) {
+  auto kern = flce_gemm_kernel<EPI, A_MN, B_MN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int total = sh.m_tiles * sh.n_tiles;
+  if (total <= 0) return cudaSuccess;
+  const int grid = total < num_sms ? total : num_sms;
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, sh, ea);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

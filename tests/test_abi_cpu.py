@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+symbol include/flce.h declares, sizes workspaces and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_cross_entropy_forward_gb300 as flce
+from linear_cross_entropy_forward_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_cross_entropy_forward_gb300.build import build
+    build()
+    return flce.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_exported_set(lib):
+    declared = _declared_functions()
+    assert declared == sorted(B.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror(lib):
+    assert lib.flce_version() == 100
+    for code in range(0, 9):
+        assert lib.flce_strerror(code)
+    assert b"unknown" in lib.flce_strerror(99)
+
+
+def test_params_struct_layout():
+    # int64 x4, int32, float, float, int32, int64 -> 56 bytes, as in flce.h
+    assert ctypes.sizeof(B.FlceParams) == 56
+    assert B.FlceParams.chunk_v.offset == 48
+
+
+def test_workspace_sizes(lib):
+    p = flce.make_params(8192, 4096, 128256, "mean", zloss_coef=1e-4)
+    fwd = flce.workspace_size(p, 0)
+    n_parts = 2 * ((128256 + 255) // 256)
+    assert fwd >= 3 * n_parts * 8192 * 4 + 3 * 8192 * 4
+    bwd = flce.workspace_size(p, 1)
+    assert bwd >= 8192 * 16  # per-row constants
+    # an explicit chunk width: dlogits chunk N*Vc*2 plus an fp32 dhidden accumulator
+    p2 = flce.make_params(300, 200, 1000, "none", chunk_v=256)
+    assert flce.workspace_size(p2, 1) >= 300 * 256 * 2 + 300 * 200 * 4
+    assert flce.kernel_launches(p2, 1) == 1 + 3 * 4
+    assert flce.kernel_launches(p2, 0) == 2
+    assert flce.kernel_launches(flce.make_params(300, 200, 1000, "sum"), 0) == 3
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=10, H=7 * 8 + 4, V=64), 3),     # H % 8
+    (dict(N=10, H=64, V=100), 3),           # V % 8
+    (dict(N=10, H=4, V=64), 2),             # H < 8
+    (dict(N=-1, H=64, V=64), 2),
+    (dict(N=10, H=64, V=0), 2),
+    (dict(N=10, H=64, V=64, chunk_v=100), 1),
+    (dict(N=10, H=64, V=64, zloss_coef=-1.0), 1),
+])
+def test_bad_params_rejected_on_host(lib, kw, code):
+    args = dict(N=10, H=64, V=64)
+    args.update(kw)
+    red = args.pop("reduction", "mean")
+    p = flce.make_params(args.pop("N"), args.pop("H"), args.pop("V"), red, **args)
+    assert lib.flce_workspace_size(ctypes.byref(p), 0) == 0
+    fake = ctypes.c_void_p(0x1000)
+    rc = lib.flce_forward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, fake,
+                          1 << 20, None)
+    assert rc == code
+    rc = lib.flce_backward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, fake,
+                           fake, fake, 1 << 20, None)
+    assert rc == code
+
+
+def test_bad_reduction_and_nulls(lib):
+    p = flce.make_params(10, 64, 64, "mean")
+    p.reduction = 7
+    assert lib.flce_forward(ctypes.byref(p), None, None, None, None, None, None, None, None,
+                            0, None) == 1
+    p = flce.make_params(10, 64, 64, "mean")
+    assert lib.flce_forward(ctypes.byref(p), None, None, None, None, None, None, None, None,
+                            0, None) == 1
+    assert lib.flce_forward(None, None, None, None, None, None, None, None, None, 0, None) == 1
+
+
+def test_misaligned_pointer_and_small_workspace(lib):
+    p = flce.make_params(10, 64, 64, "mean")
+    ok = ctypes.c_void_p(0x10000)
+    bad = ctypes.c_void_p(0x10004)
+    rc = lib.flce_forward(ctypes.byref(p), bad, ok, ok, ok, ok, ok, ok, ok, 1 << 20, None)
+    assert rc == 3
+    rc = lib.flce_forward(ctypes.byref(p), ok, ok, ok, ok, ok, ok, ok, ok, 16, None)
+    assert rc == 4
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    saved = B._lib
+    B._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            B.load_library(str(tmp_path / "nope.so"))
+    finally:
+        B._lib = saved
