@@ -24,14 +24,15 @@
 
 namespace flce {
 
+// GEMM launchers (gemm_*.cu): CTA-pair kernels, 256 x 256 tiles.
 cudaError_t launch_fwd_stats(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                             const EpiArgs&, int, cudaStream_t);
+                             const EpiArgs&, cudaStream_t);
 cudaError_t launch_bwd_dlogits(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, int, cudaStream_t);
+                               const EpiArgs&, cudaStream_t);
 cudaError_t launch_bwd_dweight(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, int, cudaStream_t);
+                               const EpiArgs&, cudaStream_t);
 cudaError_t launch_bwd_dhidden(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, int, cudaStream_t);
+                               const EpiArgs&, cudaStream_t);
 
 namespace {
 
@@ -400,7 +401,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   if (!make_map(&tmA, hidden, H, N, H, BK, BM)) return FLCE_ERR_CUDA;
   if (!make_map(&tmB, weight, V, H, V, 64, BK)) return FLCE_ERR_CUDA;
   GemmShape sh = base_shape();
-  sh.m_tiles = static_cast<int>(cdiv(N, BM));
+  sh.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
   sh.n_tiles = static_cast<int>(cdiv(V, BN));
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
   sh.raster = 0;
@@ -418,7 +419,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   ea.part_stride = N;
   ea.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
   ea.err = err;
-  if ((rc = cuda_rc(launch_fwd_stats(tmA, tmB, sh, ea, di.sms, st)))) return rc;
+  if ((rc = cuda_rc(launch_fwd_stats(tmA, tmB, sh, ea, st)))) return rc;
 
   float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
   float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
@@ -476,7 +477,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   bool ok = make_map(&mHidK, hidden, H, N, H, BK, BM) && make_map(&mWMn, weight, V, H, V, 64, BK) &&
             make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
             make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
-            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, BM) && make_map(&mWK, weight, V, H, V, BK, BN);
+            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, BM) && make_map(&mWK, weight, V, H, V, BK, 128);
   if (!ok) return FLCE_ERR_CUDA;
 
   for (int64_t c = 0; c < L.chunks; ++c) {
@@ -486,7 +487,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
 
     // dlogits[N, w] = f(hidden @ weight[:, v0:v0+w])
     GemmShape s3 = base_shape();
-    s3.m_tiles = static_cast<int>(cdiv(N, BM));
+    s3.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
     s3.n_tiles = nt;
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
     s3.raster = 0;
@@ -503,11 +504,11 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e3.dl = dl;
     e3.ld_dl = L.Vc;
     e3.err = err;
-    if ((rc = cuda_rc(launch_bwd_dlogits(mHidK, mWMn, s3, e3, di.sms, st)))) return rc;
+    if ((rc = cuda_rc(launch_bwd_dlogits(mHidK, mWMn, s3, e3, st)))) return rc;
 
     // dweight[:, v0:v0+w] = hidden^T @ dlogits
     GemmShape s4 = base_shape();
-    s4.m_tiles = static_cast<int>(cdiv(H, BM));
+    s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
     s4.n_tiles = nt;
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
     s4.raster = 0;
@@ -519,11 +520,11 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e4.out = static_cast<__nv_bfloat16*>(dweight);
     e4.ld_out = V;
     e4.err = err;
-    if ((rc = cuda_rc(launch_bwd_dweight(mHidMn, mDlMn, s4, e4, di.sms, st)))) return rc;
+    if ((rc = cuda_rc(launch_bwd_dweight(mHidMn, mDlMn, s4, e4, st)))) return rc;
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
     GemmShape s5 = base_shape();
-    s5.m_tiles = static_cast<int>(cdiv(N, BM));
+    s5.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
     s5.n_tiles = static_cast<int>(cdiv(H, BN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));
     s5.raster = 1;
@@ -540,7 +541,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
                   : c == L.chunks - 1 ? ACC_LAST
                                       : ACC_MID;
     e5.err = err;
-    if ((rc = cuda_rc(launch_bwd_dhidden(mDlK, mWK, s5, e5, di.sms, st)))) return rc;
+    if ((rc = cuda_rc(launch_bwd_dhidden(mDlK, mWK, s5, e5, st)))) return rc;
   }
   return p->validate ? read_status(ws, st) : FLCE_OK;
 }

@@ -40,6 +40,15 @@ constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // one {64 MN x 64 K} box
 
+// CTA-pair (cta_group::2) configuration: a 256 x 256 tile per pair; each CTA
+// stages its own 128 rows of A and 128 of B's 256 columns.
+constexpr int PAIR_BM = 256;
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = 128 * BK * 2;
+constexpr int PAIR_B_BYTES = 128 * BK * 2;
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + 256;
+
 enum EpiKind { EPI_FWD_STATS = 0, EPI_DLOGITS = 1, EPI_STORE_BF16 = 2, EPI_ACCUM = 3 };
 enum AccMode { ACC_FIRST = 0, ACC_MID = 1, ACC_LAST = 2, ACC_ONLY = 3 };
 
@@ -459,6 +468,228 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
   const int grid = total < num_sms ? total : num_sms;
   kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, sh, ea);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ pair kernel
+// Same roles as flce_gemm_kernel, on a cluster of two CTAs (a CTA pair):
+//   * both producers load their halves; completion is counted on the leader's
+//     (rank 0) full barrier, which expects both CTAs' bytes;
+//   * the leader's UMMA warp issues 256x256x16 cta_group::2 UMMAs and commits
+//     to the empty / tmem-full barriers of both CTAs at once (multicast);
+//   * each CTA's epilogue reads its own 128 TMEM lanes (rows) and arrives on the
+//     leader's tmem-empty barrier.
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
+                          const EpiArgs ea) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + PAIR_STAGES * PAIR_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PAIR_STAGES * PAIR_B_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + PAIR_STAGES;
+  uint64_t* tfull = bars + 2 * PAIR_STAGES;
+  uint64_t* tempty = bars + 2 * PAIR_STAGES + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * PAIR_STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_holder, TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = sh.m_tiles * sh.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        int mt, nt;
+        tile_coords(t, sh, mt, nt);
+        const int am0 = mt * PAIR_BM + static_cast<int>(rank) * 128 + sh.a_mn_off;
+        const int bn0 = nt * BN + static_cast<int>(rank) * 128 + sh.b_mn_off;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait<true>(&empty[stage], phase ^ 1u, abort_flag, ea.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+          const int k0 = kb * BK;
+          uint8_t* a = sA + stage * PAIR_A_BYTES;
+          uint8_t* b = sB + stage * PAIR_B_BYTES;
+          if constexpr (A_MN) {
+            tma_load_2d_pair(a, &tmA, fb, am0, k0 + sh.a_k_off);
+            tma_load_2d_pair(a + MN_ATOM_BYTES, &tmA, fb, am0 + 64, k0 + sh.a_k_off);
+          } else {
+            tma_load_2d_pair(a, &tmA, fb, k0 + sh.a_k_off, am0);
+          }
+          if constexpr (B_MN) {
+            tma_load_2d_pair(b, &tmB, fb, bn0, k0 + sh.b_k_off);
+            tma_load_2d_pair(b + MN_ATOM_BYTES, &tmB, fb, bn0 + 64, k0 + sh.b_k_off);
+          } else {
+            tma_load_2d_pair(b, &tmB, fb, k0 + sh.b_k_off, bn0);
+          }
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every stage this CTA filled has been released by the leader's UMMAs
+      // (their commits target this CTA's barriers, so they must land before exit)
+      for (int i = 0; i < PAIR_STAGES && ok; ++i) {
+        if (!mbar_wait<true>(&empty[stage], phase ^ 1u, abort_flag, ea.err)) break;
+        if (++stage == PAIR_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- UMMA issuer (leader CTA only)
+      constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait<true>(&tempty[acc], aph ^ 1u, abort_flag, ea.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < sh.k_blocks; ++kb) {
+          if (!mbar_wait<true>(&full[stage], phase, abort_flag, ea.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * PAIR_A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * PAIR_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            umma_bf16_pair(d_tmem, operand_desc<A_MN>(a_addr, kk, sh),
+                           operand_desc<B_MN>(b_addr, kk, sh), IDESC,
+                           (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(&empty[stage], 0x3);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(&tfull[acc], 0x3);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+    int it = 0;
+    for (int t = cid; t < total; t += ncl, ++it) {
+      int mt, nt;
+      tile_coords(t, sh, mt, nt);
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait<true>(&tfull[acc], aph, abort_flag, ea.err)) break;
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + half * 128;
+      Epilogue<EPI>::run(ea, tbase, mt * PAIR_BM + static_cast<int>(rank) * 128 + r,
+                         nt * BN + half * 128);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+// Host-side launcher of the pair kernel: clusters of 2 CTAs, as many as can be
+// resident at once (persistent), never more than there are tiles.
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmShape& sh, const EpiArgs& ea, int max_clusters,
+                             cudaStream_t stream) {
+  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int total = sh.m_tiles * sh.n_tiles;
+  if (total <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int clusters = total < max_clusters ? total : max_clusters;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, sh, ea);
+}
+
+// Largest number of co-resident CTA pairs of this kernel on the current device.
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t pair_max_clusters(int* out) {
+  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
 }
 
 }  // namespace flce
