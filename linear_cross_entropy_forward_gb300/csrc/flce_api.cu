@@ -317,10 +317,14 @@ int read_status(const void* workspace, cudaStream_t st) {
 
 inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
 
-GemmShape base_shape() {
+// a_hint / b_hint: the operand whose tiles every tile of a launch revisits keeps
+// its L2 lines (evict_last); the operand streamed through once goes first.
+GemmShape base_shape(int a_hint, int b_hint) {
   GemmShape sh{};
   sh.mn_lbo = kMnLbo;
   sh.mn_sbo = kMnSbo;
+  sh.a_hint = a_hint;
+  sh.b_hint = b_hint;
   return sh;
 }
 
@@ -400,7 +404,8 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, hidden, H, N, H, BK, BM)) return FLCE_ERR_CUDA;
   if (!make_map(&tmB, weight, V, H, V, 64, BK)) return FLCE_ERR_CUDA;
-  GemmShape sh = base_shape();
+  // hidden is revisited by every vocabulary tile; the weight streams through once
+  GemmShape sh = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
   sh.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
   sh.n_tiles = static_cast<int>(cdiv(V, BN));
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
@@ -486,7 +491,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     const int nt = static_cast<int>(cdiv(w, BN));
 
     // dlogits[N, w] = f(hidden @ weight[:, v0:v0+w])
-    GemmShape s3 = base_shape();
+    GemmShape s3 = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
     s3.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
     s3.n_tiles = nt;
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
@@ -507,7 +512,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     if ((rc = cuda_rc(launch_bwd_dlogits(mHidK, mWMn, s3, e3, st)))) return rc;
 
     // dweight[:, v0:v0+w] = hidden^T @ dlogits
-    GemmShape s4 = base_shape();
+    // hidden^T revisited by every column tile of the chunk; dlogits streamed
+    GemmShape s4 = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
     s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
     s4.n_tiles = nt;
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
@@ -523,7 +529,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     if ((rc = cuda_rc(launch_bwd_dweight(mHidMn, mDlMn, s4, e4, st)))) return rc;
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
-    GemmShape s5 = base_shape();
+    // the weight chunk is revisited by every row tile; dlogits rows streamed
+    GemmShape s5 = base_shape(L2_EVICT_FIRST, L2_EVICT_LAST);
     s5.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
     s5.n_tiles = static_cast<int>(cdiv(H, BN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));

@@ -160,6 +160,32 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Same, with an L2 eviction-priority policy (createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* map,
+                                                      uint32_t mbar_cluster_addr, int32_t x,
+                                                      int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: lines loaded with evict_last outlive evict_normal / evict_first lines.
+enum L2Hint : int { L2_NORMAL = 0, L2_EVICT_FIRST = 1, L2_EVICT_LAST = 2 };
+
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p = 0;
+  if (hint == L2_EVICT_FIRST) {
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  } else if (hint == L2_EVICT_LAST) {
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  } else {
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  }
+  return p;
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

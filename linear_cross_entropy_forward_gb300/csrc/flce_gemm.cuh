@@ -58,6 +58,7 @@ struct GemmShape {
   int a_mn_off, a_k_off;      // added to A's (mn, k) tile coordinates
   int b_mn_off, b_k_off;      // added to B's (mn, k) tile coordinates
   uint32_t mn_lbo, mn_sbo;    // descriptor strides of MN-major operands (bytes)
+  int a_hint, b_hint;         // L2 eviction priority of A / B tile loads (L2Hint)
 };
 
 struct EpiArgs {
@@ -528,6 +529,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs)
+      const uint64_t pol_a = l2_policy(sh.a_hint);
+      const uint64_t pol_b = l2_policy(sh.b_hint);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl) {
@@ -546,16 +549,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* a = sA + stage * PAIR_A_BYTES;
           uint8_t* b = sB + stage * PAIR_B_BYTES;
           if constexpr (A_MN) {
-            tma_load_2d_pair(a, &tmA, fb, am0, k0 + sh.a_k_off);
-            tma_load_2d_pair(a + MN_ATOM_BYTES, &tmA, fb, am0 + 64, k0 + sh.a_k_off);
+            tma_load_2d_pair_hint(a, &tmA, fb, am0, k0 + sh.a_k_off, pol_a);
+            tma_load_2d_pair_hint(a + MN_ATOM_BYTES, &tmA, fb, am0 + 64, k0 + sh.a_k_off, pol_a);
           } else {
-            tma_load_2d_pair(a, &tmA, fb, k0 + sh.a_k_off, am0);
+            tma_load_2d_pair_hint(a, &tmA, fb, k0 + sh.a_k_off, am0, pol_a);
           }
           if constexpr (B_MN) {
-            tma_load_2d_pair(b, &tmB, fb, bn0, k0 + sh.b_k_off);
-            tma_load_2d_pair(b + MN_ATOM_BYTES, &tmB, fb, bn0 + 64, k0 + sh.b_k_off);
+            tma_load_2d_pair_hint(b, &tmB, fb, bn0, k0 + sh.b_k_off, pol_b);
+            tma_load_2d_pair_hint(b + MN_ATOM_BYTES, &tmB, fb, bn0 + 64, k0 + sh.b_k_off, pol_b);
           } else {
-            tma_load_2d_pair(b, &tmB, fb, k0 + sh.b_k_off, bn0);
+            tma_load_2d_pair_hint(b, &tmB, fb, k0 + sh.b_k_off, bn0, pol_b);
           }
           if (++stage == PAIR_STAGES) {
             stage = 0;

@@ -1,0 +1,140 @@
+"""Full-size parity in the launch configuration bench.py times (default chunking).
+
+Per-token loss / entropy / lse / E_p[z] and dhidden rows are compared with the fp64
+oracle on seeded row samples (each needs only its own row of logits).  Reduced
+outputs are checked by the property reduced == mean/sum of the per-token outputs,
+and dweight by the zero row sum that holds without soft-cap and z-loss
+(sum_v dlogits[n, v] = 0 for every row).  The Llama-2 head shape is also compared
+element by element against the complete oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_forward_gb300 import flce_backward, flce_forward
+from linear_cross_entropy_forward_gb300 import workloads as wl
+from oracle import flce_oracle as orc
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOK_ABS = 2e-3
+RED_REL = 1e-4
+GRAD_REL_L2 = 1e-2
+N_SAMPLE = 48
+
+FULL = [wl.LLAMA2, wl.LLAMA3, wl.GEMMA2, wl.QWEN25]
+
+
+def _cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_cross_entropy_forward_gb300.build import build
+    build()
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def sample_rows(w, labels):
+    rng = np.random.default_rng(1234)
+    y = labels.numpy()
+    ign = np.nonzero(y == wl.IGNORE_INDEX)[0]
+    val = np.nonzero(y != wl.IGNORE_INDEX)[0]
+    pick = list(rng.choice(val, size=N_SAMPLE - 4, replace=False))
+    if ign.size:
+        pick += list(rng.choice(ign, size=min(4, ign.size), replace=False))
+    # the first and last rows exercise the edge tiles
+    pick += [0, w.N - 1]
+    return np.unique(np.array(pick, dtype=np.int64))
+
+
+@pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
+def test_fullsize_sampled_parity(w):
+    _cuda_or_skip()
+    dev = torch.device("cuda")
+    label_dev = "cuda" if w.label_mode == "self" else "cpu"
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w, label_device=label_dev)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True, **kw)
+    dh, dw = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
+                           validate=True, **kw)
+    if w.reduction != "none":
+        loss_t, ent_t, _, _ = flce_forward(hd, Wd, yd, "none", validate=True, **kw)
+    else:
+        loss_t, ent_t = loss, ent
+    torch.cuda.synchronize()
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    g_lse, g_ez, g_lt, g_et = f64(lse), f64(ez), f64(loss_t), f64(ent_t)
+    valid = labels.numpy() != wl.IGNORE_INDEX
+    for name, arr in (("lse", g_lse), ("ez", g_ez), ("loss", g_lt), ("ent", g_et)):
+        assert np.all(np.isfinite(arr)), name
+    assert np.all(g_lt[~valid] == 0) and np.all(g_et[~valid] == 0)
+
+    # reduced outputs are the mean / sum of the per-token outputs (property at any size)
+    if w.reduction != "none":
+        n_valid = valid.sum()
+        s_l, s_e = g_lt.sum(), g_et.sum()
+        if w.reduction == "mean":
+            s_l, s_e = s_l / n_valid, s_e / n_valid
+        assert abs(float(loss.item()) - s_l) <= RED_REL * abs(s_l)
+        assert abs(float(ent.item()) - s_e) <= RED_REL * abs(s_e)
+
+    # oracle on sampled rows
+    rows = sample_rows(w, labels)
+    h64 = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
+    W64 = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
+    y = labels.numpy()
+    o = orc.forward(h64[rows], W64, y[rows], "none", **kw)
+    assert np.abs(g_lse[rows] - o["lse"]).max() <= TOK_ABS
+    assert np.abs(g_ez[rows] - o["ez"]).max() <= TOK_ABS
+    assert np.abs(g_lt[rows] - o["loss_tok"]).max() <= TOK_ABS
+    assert np.abs(g_et[rows] - o["entropy_tok"]).max() <= TOK_ABS
+    lse_full = np.zeros(w.N)
+    ez_full = np.zeros(w.N)
+    lse_full[rows] = o["lse"]
+    ez_full[rows] = o["ez"]
+    dh_o, _ = orc.backward(h64, W64, y, lse_full, ez_full, g_loss.numpy(), g_ent.numpy(),
+                           w.reduction, rows=rows, **kw)
+    dh_rows = f64(dh[torch.from_numpy(rows).to(dev)])
+    assert rel_l2(dh_rows, dh_o) <= GRAD_REL_L2
+    # every ignored row of dhidden is exactly zero
+    ign = torch.from_numpy(np.nonzero(~valid)[0]).to(dev)
+    if ign.numel():
+        assert torch.all(dh[ign].view(torch.int16) == 0)
+
+    # dweight: finite everywhere; zero row sums when neither soft-cap nor z-loss is on
+    dwf = dw.float()
+    assert torch.isfinite(dwf).all()
+    if w.softcap == 0 and w.zloss_coef == 0:
+        rs = dwf.double().sum(dim=1)
+        ratio = float(rs.norm() / (dwf.double().norm() * np.sqrt(w.V)))
+        # a dweight without the zero-sum structure gives ratio ~ 1/sqrt(V); bf16 rounding
+        # of dlogits and of dweight leaves ~2^-9/sqrt(V)
+        assert ratio <= 0.05 / np.sqrt(w.V), ratio
+
+
+def test_llama2_head_against_complete_oracle():
+    """Llama-2-7B head shape: every output element against the full fp64 oracle."""
+    _cuda_or_skip()
+    w = wl.LLAMA2
+    dev = torch.device("cuda")
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True)
+    dh, dw = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
+                           validate=True)
+    torch.cuda.synchronize()
+    h64 = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
+    W64 = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
+    y = labels.numpy()
+    o = orc.forward(h64, W64, y, w.reduction)
+    dh_o, dw_o = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.numpy(), g_ent.numpy(),
+                              w.reduction)
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    assert np.abs(f64(loss) - o["loss"]).max() <= TOK_ABS
+    assert np.abs(f64(ent) - o["entropy"]).max() <= TOK_ABS
+    assert np.abs(f64(lse) - o["lse"]).max() <= TOK_ABS
+    assert rel_l2(f64(dh), dh_o) <= GRAD_REL_L2
+    assert rel_l2(f64(dw), dw_o) <= GRAD_REL_L2
