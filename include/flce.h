@@ -66,7 +66,8 @@ enum {
   FLCE_ERR_LABEL = 5,         /* a label outside [0, V) that is not ignore_index */
   FLCE_ERR_TIMEOUT = 6,       /* a device pipeline wait exceeded its time limit */
   FLCE_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed */
-  FLCE_ERR_DEVICE = 8         /* current device is not an sm_103 GPU */
+  FLCE_ERR_DEVICE = 8,        /* current device is not an sm_103 GPU */
+  FLCE_ERR_SCRATCH_LIMIT = 9  /* problem needs more than FLCE_NOALLOC_SCRATCH_BYTES */
 };
 
 typedef struct {
@@ -119,6 +120,26 @@ int flce_kernel_launches(const flce_params* params, int phase);
 
 /* Static, NUL-terminated description of a status code. */
 const char* flce_strerror(int code);
+
+/* Forward pass for callers that cannot allocate device memory.  (The pages have
+ * no counterpart: this entry point serves callers that can't call cudaMalloc,
+ * e.g. code running during CUDA graph capture or under an allocator they do not
+ * control, which therefore cannot provide the workspace flce_forward needs.)
+ *   Same arguments and results as flce_forward, minus the workspace.  The scratch
+ *   it uses is a static device array of FLCE_NOALLOC_SCRATCH_BYTES (64 MiB) held
+ *   by every GPU that loads the library until the process exits; problems whose
+ *   flce_workspace_size(params, 0) exceeds it return FLCE_ERR_SCRATCH_LIMIT
+ *   without enqueueing anything.  Nothing is allocated (no cudaMalloc/cudaFree).
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.  All calls
+ *   share the array (its header is cleared on every call; the rest is fully
+ *   rewritten), so calls that may overlap on the GPU -- other streams, other
+ *   threads -- race and must be serialised by the caller.  flce_status() is not
+ *   available for it; set params->validate to get device-side errors returned. */
+#define FLCE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int flce_forward_noalloc(const flce_params* params, const void* hidden, const void* weight,
+                         const int64_t* labels, float* loss, float* entropy, float* lse,
+                         float* ez, void* stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int flce_version(void);

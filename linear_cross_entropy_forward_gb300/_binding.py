@@ -40,7 +40,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
-            "flce_kernel_launches", "flce_strerror", "flce_version")
+            "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:

@@ -348,6 +348,8 @@ const char* flce_strerror(int code) {
     case FLCE_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FLCE_ERR_CUDA: return "CUDA call failed";
     case FLCE_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case FLCE_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than flce_forward_noalloc's static 64 MiB array";
     default: return "unknown status";
   }
 }
