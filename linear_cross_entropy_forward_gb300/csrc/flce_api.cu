@@ -24,7 +24,7 @@
 
 namespace flce {
 
-// GEMM launchers (gemm_*.cu): CTA-pair kernels, 256 x 256 tiles.
+// GEMM launchers (gemm_*.cu): CTA-pair kernels on 256 x TN tiles.
 cudaError_t launch_fwd_stats(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
                              const EpiArgs&, cudaStream_t);
 cudaError_t launch_bwd_dlogits(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
@@ -184,7 +184,7 @@ struct FwdLayout {
 
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
-  L.n_parts = 2 * cdiv(p->V, BN);
+  L.n_parts = 2 * cdiv(p->V, TN_FWD);  // one part per TN_FWD/2 columns
   const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * p->N) * 4);
   const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
   size_t off = kHeaderBytes;
@@ -204,13 +204,14 @@ struct BwdLayout {
 };
 
 int64_t chunk_width(const flce_params* p) {
-  const int64_t vfull = cdiv(p->V, BN) * BN;
+  constexpr int64_t kAlign = 256;  // chunk widths are whole tiles of every kernel
+  const int64_t vfull = cdiv(p->V, kAlign) * kAlign;
   int64_t vc = p->chunk_v;
   if (vc <= 0) {
     const int64_t n = p->N > 0 ? p->N : 1;
-    vc = (kDefaultChunkBytes / (2 * n)) / BN * BN;
+    vc = (kDefaultChunkBytes / (2 * n)) / kAlign * kAlign;
   }
-  if (vc < BN) vc = BN;
+  if (vc < kAlign) vc = kAlign;
   if (vc > vfull) vc = vfull;
   return vc;
 }
@@ -235,9 +236,9 @@ int check_params(const flce_params* p) {
   if (p->N < 0 || p->H < 8 || p->V < 1) return FLCE_ERR_BAD_SHAPE;
   if (p->N > kMaxDim || p->H > kMaxDim || p->V > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   if (p->H % 8 != 0 || p->V % 8 != 0) return FLCE_ERR_ALIGN;
-  if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % BN != 0)) return FLCE_ERR_BAD_ARG;
+  if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % 256 != 0)) return FLCE_ERR_BAD_ARG;
   // chunk-relative and vocabulary column indices are 32-bit inside the kernels
-  if (cdiv(p->V, BN) * BN > kMaxDim) return FLCE_ERR_BAD_SHAPE;
+  if (cdiv(p->V, 256) * 256 > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   return FLCE_OK;
 }
 
@@ -317,10 +318,26 @@ int read_status(const void* workspace, cudaStream_t st) {
 
 inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
 
-// a_hint / b_hint: the operand whose tiles every tile of a launch revisits keeps
-// its L2 lines (evict_last); the operand streamed through once goes first.
+// a_hint / b_hint: the operand whose panels every tile of a group revisits keeps
+// its L2 lines (evict_last).  The streamed operand keeps the normal policy: with
+// evict_first its tiles left L2 before all the tiles sharing them had read them.
+#ifndef FLCE_L2_PANEL_BUDGET
+#define FLCE_L2_PANEL_BUDGET (int64_t(40) << 20)
+#endif
+
+// Tiles of the fast raster dimension per group so that the panels of the operand
+// every tile revisits (each `panel_bytes` long) stay within an L2 budget; the
+// other operand is then streamed once per group.
+int raster_group(int64_t panel_bytes, int fast_tiles) {
+  if (FLCE_L2_PANEL_BUDGET <= 0 || panel_bytes <= 0) return fast_tiles;
+  int64_t g = FLCE_L2_PANEL_BUDGET / panel_bytes;
+  if (g < 1) g = 1;
+  return g < fast_tiles ? static_cast<int>(g) : fast_tiles;
+}
+
 GemmShape base_shape(int a_hint, int b_hint) {
   GemmShape sh{};
+  sh.group = 1 << 30;
   sh.mn_lbo = kMnLbo;
   sh.mn_sbo = kMnSbo;
   sh.a_hint = a_hint;
@@ -404,14 +421,15 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   }
 
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, hidden, H, N, H, BK, BM)) return FLCE_ERR_CUDA;
+  if (!make_map(&tmA, hidden, H, N, H, BK, 128)) return FLCE_ERR_CUDA;
   if (!make_map(&tmB, weight, V, H, V, 64, BK)) return FLCE_ERR_CUDA;
-  // hidden is revisited by every vocabulary tile; the weight streams through once
-  GemmShape sh = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
+  // hidden is revisited by every vocabulary tile of its group; the weight streams
+  GemmShape sh = base_shape(L2_EVICT_LAST, L2_NORMAL);
   sh.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
-  sh.n_tiles = static_cast<int>(cdiv(V, BN));
+  sh.n_tiles = static_cast<int>(cdiv(V, TN_FWD));
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
   sh.raster = 0;
+  sh.group = raster_group(int64_t(PAIR_BM) * H * 2, sh.m_tiles);
   EpiArgs ea{};
   ea.rows = static_cast<int>(N);
   ea.cols = static_cast<int>(V);
@@ -481,23 +499,24 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   if ((rc = cuda_rc(cudaGetLastError()))) return rc;
 
   CUtensorMap mHidK, mWMn, mHidMn, mDlMn, mDlK, mWK;
-  bool ok = make_map(&mHidK, hidden, H, N, H, BK, BM) && make_map(&mWMn, weight, V, H, V, 64, BK) &&
+  bool ok = make_map(&mHidK, hidden, H, N, H, BK, 128) && make_map(&mWMn, weight, V, H, V, 64, BK) &&
             make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
             make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
-            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, BM) && make_map(&mWK, weight, V, H, V, BK, 128);
+            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, 128) &&
+            make_map(&mWK, weight, V, H, V, BK, TN_DHIDDEN / 2);
   if (!ok) return FLCE_ERR_CUDA;
 
   for (int64_t c = 0; c < L.chunks; ++c) {
     const int64_t v0 = c * L.Vc;
     const int64_t w = (V - v0) < L.Vc ? (V - v0) : L.Vc;
-    const int nt = static_cast<int>(cdiv(w, BN));
 
     // dlogits[N, w] = f(hidden @ weight[:, v0:v0+w])
-    GemmShape s3 = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
+    GemmShape s3 = base_shape(L2_EVICT_LAST, L2_NORMAL);
     s3.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
-    s3.n_tiles = nt;
+    s3.n_tiles = static_cast<int>(cdiv(w, TN_DLOGITS));
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
     s3.raster = 0;
+    s3.group = raster_group(int64_t(PAIR_BM) * H * 2, s3.m_tiles);
     s3.b_mn_off = static_cast<int>(v0);
     EpiArgs e3{};
     e3.rows = static_cast<int>(N);
@@ -515,11 +534,12 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
 
     // dweight[:, v0:v0+w] = hidden^T @ dlogits
     // hidden^T revisited by every column tile of the chunk; dlogits streamed
-    GemmShape s4 = base_shape(L2_EVICT_LAST, L2_EVICT_FIRST);
+    GemmShape s4 = base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
-    s4.n_tiles = nt;
+    s4.n_tiles = static_cast<int>(cdiv(w, TN_DWEIGHT));
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
     s4.raster = 0;
+    s4.group = raster_group(int64_t(PAIR_BM) * N * 2, s4.m_tiles);
     EpiArgs e4{};
     e4.rows = static_cast<int>(H);
     e4.cols = static_cast<int>(w);
@@ -532,11 +552,12 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
     // the weight chunk is revisited by every row tile; dlogits rows streamed
-    GemmShape s5 = base_shape(L2_EVICT_FIRST, L2_EVICT_LAST);
+    GemmShape s5 = base_shape(L2_NORMAL, L2_EVICT_LAST);
     s5.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
-    s5.n_tiles = static_cast<int>(cdiv(H, BN));
+    s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));
     s5.raster = 1;
+    s5.group = raster_group(int64_t(TN_DHIDDEN) * w * 2, s5.n_tiles);
     s5.b_k_off = static_cast<int>(v0);
     EpiArgs e5{};
     e5.rows = static_cast<int>(N);

@@ -2,13 +2,17 @@
 // linear cross-entropy + entropy path (verl PR #462, "Equivalent compute logic":
 // logits = hidden @ weight are never stored; every use of them is fused here).
 //
-//   warp 0      TMA producer: bf16 tiles of A (BM x BK) and B (BN x BK) into a
-//               STAGES-deep ring of 128B-swizzled shared-memory buffers.
-//   warp 1      UMMA issuer: 128x256x16 tcgen05.mma into one of two 256-column
-//               fp32 TMEM accumulators (double buffered against the epilogue).
-//   warps 2..9  epilogue: tcgen05.ld one row per thread (warp w reads TMEM lanes
-//               32*(w%4)..+31, columns half (w-2)/4 of the tile), then one of:
-//     EPI_FWD_STATS  online-softmax partials per row and 128-column block:
+// A cluster of two CTAs (a CTA pair) owns 256 x TN output tiles:
+//   warp 0      TMA producer (both CTAs): this CTA's 128 rows of A and TN/2
+//               columns of B into a ring of 128B-swizzled shared-memory stages;
+//               completion is counted on the leader CTA's (rank 0) full barrier.
+//   warp 1      UMMA issuer (leader only): 256 x TN x 16 tcgen05.mma.cta_group::2
+//               into one of 512/TN fp32 TMEM accumulators, commits multicast to
+//               the barriers of both CTAs.
+//   warps 2..9  epilogue (both CTAs): tcgen05.ld one row per thread (warp w reads
+//               TMEM lanes 32*(w%4)..+31 and column half (w-2)/4 of the tile),
+//               then one of:
+//     EPI_FWD_STATS  online-softmax partials per row and TN/2-column block:
 //                    running max m, sum-exp d and centred s = sum e^{u-m}(u-m)
 //                    in log2 units, plus the label logit (Liger-Kernel PR #551:
 //                    m and d of the online softmax feed the entropy).
@@ -26,35 +30,59 @@
 
 namespace flce {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int UK = 16;  // K of one kind::f16 UMMA
-constexpr int STAGES = 4;
-constexpr int A_TILE_BYTES = BM * BK * 2;
-constexpr int B_TILE_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int PAIR_BM = 256;  // rows of a pair tile (128 per CTA)
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int TMEM_COLS = 512;
 constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // one {64 MN x 64 K} box
+constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
 
-// CTA-pair (cta_group::2) configuration: a 256 x 256 tile per pair; each CTA
-// stages its own 128 rows of A and 128 of B's 256 columns.
-constexpr int PAIR_BM = 256;
-constexpr int PAIR_STAGES = 6;
-constexpr int PAIR_A_BYTES = 128 * BK * 2;
-constexpr int PAIR_B_BYTES = 128 * BK * 2;
-constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
-constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + 256;
+// Per-tile-width configuration of the pair kernel.
+template <int TN>
+struct PairCfg {
+  static_assert(TN == 128 || TN == 256, "tile width");
+  static constexpr int B_ROWS = TN / 2;                // this CTA's share of B's columns
+  static constexpr int A_BYTES = 128 * BK * 2;         // 16 KB
+  static constexpr int B_BYTES = B_ROWS * BK * 2;      // 8 or 16 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NACC = TMEM_COLS / TN;          // TMEM accumulators
+  static constexpr int EPI_COLS = TN / 2;              // columns per epilogue warp
+  static constexpr int EPI_CHUNKS = EPI_COLS / 32;     // tcgen05.ld x32 per warp per tile
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 9 ? 9 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+  static_assert((2 * STAGES + 2 * NACC) * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+// Tile width (UMMA N) of each kernel of the path.
+#ifndef FLCE_TN_FWD
+#define FLCE_TN_FWD 256
+#endif
+#ifndef FLCE_TN_DLOGITS
+#define FLCE_TN_DLOGITS 256
+#endif
+#ifndef FLCE_TN_DWEIGHT
+#define FLCE_TN_DWEIGHT 256
+#endif
+#ifndef FLCE_TN_DHIDDEN
+#define FLCE_TN_DHIDDEN 256
+#endif
+constexpr int TN_FWD = FLCE_TN_FWD;
+constexpr int TN_DLOGITS = FLCE_TN_DLOGITS;
+constexpr int TN_DWEIGHT = FLCE_TN_DWEIGHT;
+constexpr int TN_DHIDDEN = FLCE_TN_DHIDDEN;
 
 enum EpiKind { EPI_FWD_STATS = 0, EPI_DLOGITS = 1, EPI_STORE_BF16 = 2, EPI_ACCUM = 3 };
 enum AccMode { ACC_FIRST = 0, ACC_MID = 1, ACC_LAST = 2, ACC_ONLY = 3 };
 
 struct GemmShape {
   int m_tiles, n_tiles, k_blocks;
-  int raster;                 // 0: m fastest, 1: n fastest
+  int raster;                 // 0: m fastest, 1: n fastest (within a group)
+  int group;                  // tiles of the fast dimension per group (see tile_coords)
   int a_mn_off, a_k_off;      // added to A's (mn, k) tile coordinates
   int b_mn_off, b_k_off;      // added to B's (mn, k) tile coordinates
   uint32_t mn_lbo, mn_sbo;    // descriptor strides of MN-major operands (bytes)
@@ -73,7 +101,7 @@ struct EpiArgs {
   float* pm;
   float* pd;
   float* ps;
-  int64_t part_stride;  // elements between consecutive 128-column parts
+  int64_t part_stride;  // elements between consecutive column parts
   float* zlabel;
   // EPI_DLOGITS
   const float4* rowc;   // per row: (lse*log2e, a(1+2 coef lse) + b Ez, b, a)
@@ -90,26 +118,24 @@ struct EpiArgs {
   uint32_t* err;
 };
 
+// Tile order.  raster 0: groups of `group` consecutive m-tiles, m fastest within
+// a group, every n-tile of the group before the next group (group >= m_tiles:
+// plain m-fastest order).  raster 1: the same with the roles of m and n swapped.
+// Grouping bounds how much of the operand revisited by every tile must stay in L2.
 __device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int& mt, int& nt) {
-  if (sh.raster == 0) {
-    mt = t % sh.m_tiles;
-    nt = t / sh.m_tiles;
-  } else {
-    nt = t % sh.n_tiles;
-    mt = t / sh.n_tiles;
-  }
-}
-
-template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                             int mn0, int k0) {
-  if constexpr (!MN) {
-    tma_load_2d(dst, map, bar, k0, mn0);
-  } else {
-#pragma unroll
-    for (int j = 0; j < ROWS / 64; ++j)
-      tma_load_2d(dst + j * MN_ATOM_BYTES, map, bar, mn0 + 64 * j, k0);
-  }
+  const bool m_major = sh.raster == 0;
+  const int fast_tiles = m_major ? sh.m_tiles : sh.n_tiles;
+  const int slow_tiles = m_major ? sh.n_tiles : sh.m_tiles;
+  const int g = sh.group < fast_tiles ? sh.group : fast_tiles;
+  const int per_group = g * slow_tiles;
+  const int grp = t / per_group;
+  const int r = t - grp * per_group;
+  const int rem = fast_tiles - grp * g;
+  const int gsize = rem < g ? rem : g;
+  const int f = grp * g + r % gsize;
+  const int sl = r / gsize;
+  mt = m_major ? f : sl;
+  nt = m_major ? sl : f;
 }
 
 template <bool MN>
@@ -125,12 +151,15 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, const Ge
 }
 
 // ------------------------------------------------------------------ epilogues
+// Each epilogue thread owns one row `row` and CH * 32 consecutive columns
+// starting at problem column `col0`; `tbase` addresses them in TMEM.
 template <int EPI>
 struct Epilogue;
 
-// Online-softmax partial statistics of one row over 128 columns.
+// Online-softmax partial statistics of one row over its CH*32 columns.
 template <>
 struct Epilogue<EPI_FWD_STATS> {
+  template <int CH>
   static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
                                              int col0) {
     const bool row_ok = row < ea.rows;
@@ -145,7 +174,7 @@ struct Epilogue<EPI_FWD_STATS> {
     float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f;
     bool hit = false;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CH; ++c) {
       float x[32];
       tmem_ld32(tbase + c * 32, x);
       const int vb = vcol0 + c * 32;
@@ -188,7 +217,7 @@ struct Epilogue<EPI_FWD_STATS> {
       }
     }
     if (row_ok) {
-      const int64_t part = vcol0 / 128;
+      const int64_t part = vcol0 / (CH * 32);
       const int64_t o = part * ea.part_stride + row;
       ea.pm[o] = mx;
       ea.pd[o] = d;
@@ -198,9 +227,10 @@ struct Epilogue<EPI_FWD_STATS> {
   }
 };
 
-// dlogits of one row over 128 columns of the current vocabulary chunk.
+// dlogits of one row over its columns of the current vocabulary chunk.
 template <>
 struct Epilogue<EPI_DLOGITS> {
+  template <int CH>
   static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
                                              int col0) {
     const bool row_ok = row < ea.rows;
@@ -216,7 +246,7 @@ struct Epilogue<EPI_DLOGITS> {
     const int vcol0 = ea.col_base + col0;
     __nv_bfloat16* dst = ea.dl + static_cast<int64_t>(row) * ea.ld_dl + col0;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CH; ++c) {
       float x[32];
       tmem_ld32(tbase + c * 32, x);
       const int vb = vcol0 + c * 32;
@@ -251,15 +281,16 @@ struct Epilogue<EPI_DLOGITS> {
   }
 };
 
-// bf16 store of a 128-column row segment (dweight).
+// bf16 store of a row segment (dweight).
 template <>
 struct Epilogue<EPI_STORE_BF16> {
+  template <int CH>
   static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
                                              int col0) {
     const bool row_ok = row < ea.rows;
     __nv_bfloat16* dst = ea.out + static_cast<int64_t>(row) * ea.ld_out + ea.col_base + col0;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CH; ++c) {
       float x[32];
       tmem_ld32(tbase + c * 32, x);
       if (!row_ok) continue;
@@ -281,12 +312,13 @@ struct Epilogue<EPI_STORE_BF16> {
 // fp32 accumulation across vocabulary chunks (dhidden).
 template <>
 struct Epilogue<EPI_ACCUM> {
+  template <int CH>
   static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
                                              int col0) {
     const bool row_ok = row < ea.rows;
     const int64_t base = static_cast<int64_t>(row) * ea.ld_acc + col0;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CH; ++c) {
       float x[32];
       tmem_ld32(tbase + c * 32, x);
       if (!row_ok) continue;
@@ -317,184 +349,29 @@ struct Epilogue<EPI_ACCUM> {
   }
 };
 
-// ------------------------------------------------------------------ kernel
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
-                     const EpiArgs ea) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], NUM_EPI_WARPS);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
-
-  const int total = sh.m_tiles * sh.n_tiles;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer
-      uint32_t stage = 0, phase = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        int mt, nt;
-        tile_coords(t, sh, mt, nt);
-        bool ok = true;
-        for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ea.err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          const int k0 = kb * BK;
-          load_operand<A_MN, BM>(sA + stage * A_TILE_BYTES, &tmA, &full[stage],
-                                 mt * BM + sh.a_mn_off, k0 + sh.a_k_off);
-          load_operand<B_MN, BN>(sB + stage * B_TILE_BYTES, &tmB, &full[stage],
-                                 nt * BN + sh.b_mn_off, k0 + sh.b_k_off);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- UMMA issuer
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-      uint32_t stage = 0, phase = 0;
-      int it = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, ea.err)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        bool ok = true;
-        for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, ea.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / UK; ++kk) {
-            umma_bf16(d_tmem, operand_desc<A_MN>(a_addr, kk, sh),
-                      operand_desc<B_MN>(b_addr, kk, sh), IDESC, (kb | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(&tfull[acc]);
-      }
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue warps
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int r = q * 32 + lane;
-    int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      int mt, nt;
-      tile_coords(t, sh, mt, nt);
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aph, abort_flag, ea.err)) break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + half * 128;
-      Epilogue<EPI>::run(ea, tbase, mt * BM + r, nt * BN + half * 128);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
-// Host-side launcher, instantiated in the gemm_*.cu translation units.
-template <int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh,
-                        const EpiArgs& ea, int num_sms, cudaStream_t stream) {
-  auto kern = flce_gemm_kernel<EPI, A_MN, B_MN>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const int total = sh.m_tiles * sh.n_tiles;
-  if (total <= 0) return cudaSuccess;
-  const int grid = total < num_sms ? total : num_sms;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, sh, ea);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ pair kernel
-// Same roles as flce_gemm_kernel, on a cluster of two CTAs (a CTA pair):
-//   * both producers load their halves; completion is counted on the leader's
-//     (rank 0) full barrier, which expects both CTAs' bytes;
-//   * the leader's UMMA warp issues 256x256x16 cta_group::2 UMMAs and commits
-//     to the empty / tmem-full barriers of both CTAs at once (multicast);
-//   * each CTA's epilogue reads its own 128 TMEM lanes (rows) and arrives on the
-//     leader's tmem-empty barrier.
-template <int EPI, bool A_MN, bool B_MN>
+// Both producers load their halves; completion is counted on the leader's full
+// barrier, which expects both CTAs' bytes.  The leader's UMMA warp commits to the
+// empty / tmem-full barriers of both CTAs at once (multicast).  Each CTA's
+// epilogue reads its own 128 TMEM lanes (rows) and arrives on the leader's
+// tmem-empty barrier.
+template <int EPI, bool A_MN, bool B_MN, int TN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
                           const EpiArgs ea) {
+  using C = PairCfg<TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + PAIR_STAGES * PAIR_A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PAIR_STAGES * PAIR_B_BYTES);
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
   uint64_t* full = bars;
-  uint64_t* empty = bars + PAIR_STAGES;
-  uint64_t* tfull = bars + 2 * PAIR_STAGES;
-  uint64_t* tempty = bars + 2 * PAIR_STAGES + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * PAIR_STAGES + 4);
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = bars + 2 * C::STAGES + C::NACC;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 2 * C::NACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -504,11 +381,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int ncl = static_cast<int>(cluster_count_x());
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PAIR_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 2 * NUM_EPI_WARPS);
     }
@@ -537,17 +414,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int mt, nt;
         tile_coords(t, sh, mt, nt);
         const int am0 = mt * PAIR_BM + static_cast<int>(rank) * 128 + sh.a_mn_off;
-        const int bn0 = nt * BN + static_cast<int>(rank) * 128 + sh.b_mn_off;
+        const int bn0 = nt * TN + static_cast<int>(rank) * C::B_ROWS + sh.b_mn_off;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait<true>(&empty[stage], phase ^ 1u, abort_flag, ea.err)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ea.err)) {
             ok = false;
             break;
           }
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           const int k0 = kb * BK;
-          uint8_t* a = sA + stage * PAIR_A_BYTES;
-          uint8_t* b = sB + stage * PAIR_B_BYTES;
+          uint8_t* a = sA + stage * C::A_BYTES;
+          uint8_t* b = sB + stage * C::B_BYTES;
           if constexpr (A_MN) {
             tma_load_2d_pair_hint(a, &tmA, fb, am0, k0 + sh.a_k_off, pol_a);
             tma_load_2d_pair_hint(a + MN_ATOM_BYTES, &tmA, fb, am0 + 64, k0 + sh.a_k_off, pol_a);
@@ -555,12 +432,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d_pair_hint(a, &tmA, fb, k0 + sh.a_k_off, am0, pol_a);
           }
           if constexpr (B_MN) {
-            tma_load_2d_pair_hint(b, &tmB, fb, bn0, k0 + sh.b_k_off, pol_b);
-            tma_load_2d_pair_hint(b + MN_ATOM_BYTES, &tmB, fb, bn0 + 64, k0 + sh.b_k_off, pol_b);
+#pragma unroll
+            for (int j = 0; j < C::B_ROWS / 64; ++j)
+              tma_load_2d_pair_hint(b + j * MN_ATOM_BYTES, &tmB, fb, bn0 + 64 * j,
+                                    k0 + sh.b_k_off, pol_b);
           } else {
             tma_load_2d_pair_hint(b, &tmB, fb, k0 + sh.b_k_off, bn0, pol_b);
           }
-          if (++stage == PAIR_STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -568,9 +447,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // drain: every stage this CTA filled has been released by the leader's UMMAs
       // (their commits target this CTA's barriers, so they must land before exit)
-      for (int i = 0; i < PAIR_STAGES && ok; ++i) {
-        if (!mbar_wait<true>(&empty[stage], phase ^ 1u, abort_flag, ea.err)) break;
-        if (++stage == PAIR_STAGES) {
+      for (int i = 0; i < C::STAGES && ok; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ea.err)) break;
+        if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
@@ -580,32 +459,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- UMMA issuer (leader CTA only)
-      constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, TN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl, ++it) {
-        const int acc = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
+        const int acc = it % C::NACC;
+        const uint32_t aph = (it / C::NACC) & 1;
+        // the epilogues of both CTAs arrive here (cluster-scope acquire)
         if (!mbar_wait<true>(&tempty[acc], aph ^ 1u, abort_flag, ea.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * TN;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
-          if (!mbar_wait<true>(&full[stage], phase, abort_flag, ea.err)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, ea.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * PAIR_A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * PAIR_B_BYTES);
+          const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
+          uint64_t ad[BK / UK], bd[BK / UK];
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            umma_bf16_pair(d_tmem, operand_desc<A_MN>(a_addr, kk, sh),
-                           operand_desc<B_MN>(b_addr, kk, sh), IDESC,
-                           (kb | kk) != 0 ? 1u : 0u);
+            ad[kk] = operand_desc<A_MN>(a_addr, kk, sh);
+            bd[kk] = operand_desc<B_MN>(b_addr, kk, sh);
           }
+          umma_bf16_pair_x4(d_tmem, ad, bd, IDESC, kb != 0 ? 1u : 0u);
           umma_commit_pair(&empty[stage], 0x3);
-          if (++stage == PAIR_STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -624,14 +505,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int t = cid; t < total; t += ncl, ++it) {
       int mt, nt;
       tile_coords(t, sh, mt, nt);
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait<true>(&tfull[acc], aph, abort_flag, ea.err)) break;
+      const int acc = it % C::NACC;
+      const uint32_t aph = (it / C::NACC) & 1;
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, ea.err)) break;
       tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + half * 128;
-      Epilogue<EPI>::run(ea, tbase, mt * PAIR_BM + static_cast<int>(rank) * 128 + r,
-                         nt * BN + half * 128);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TN +
+                             half * C::EPI_COLS;
+      Epilogue<EPI>::template run<C::EPI_CHUNKS>(
+          ea, tbase, mt * PAIR_BM + static_cast<int>(rank) * 128 + r,
+          nt * TN + half * C::EPI_COLS);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -647,13 +529,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // Host-side launcher of the pair kernel: clusters of 2 CTAs, as many as can be
 // resident at once (persistent), never more than there are tiles.
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmShape& sh, const EpiArgs& ea, int max_clusters,
                              cudaStream_t stream) {
-  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN>;
+  using C = PairCfg<TN>;
+  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN, TN>;
   cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int total = sh.m_tiles * sh.n_tiles;
   if (total <= 0) return cudaSuccess;
@@ -664,7 +547,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -674,13 +557,13 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
 }
 
 // Largest number of co-resident CTA pairs of this kernel on the current device.
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t pair_max_clusters(int* out) {
-  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN>;
+  using C = PairCfg<TN>;
+  auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN, TN>;
   cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -689,7 +572,7 @@ cudaError_t pair_max_clusters(int* out) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(out, kern, &cfg);

@@ -14,12 +14,12 @@ cudaError_t launch_bwd_dhidden(const CUtensorMap& tmA, const CUtensorMap& tmB, c
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   int mc = max_clusters[dev].load();
   if (mc <= 0) {
-    e = pair_max_clusters<EPI_ACCUM, false, false>(&mc);
+    e = pair_max_clusters<EPI_ACCUM, false, false, TN_DHIDDEN>(&mc);
     if (e != cudaSuccess) return e;
     if (mc <= 0) return cudaErrorInvalidConfiguration;
     max_clusters[dev].store(mc);
   }
-  return launch_gemm_pair<EPI_ACCUM, false, false>(tmA, tmB, sh, ea, mc, stream);
+  return launch_gemm_pair<EPI_ACCUM, false, false, TN_DHIDDEN>(tmA, tmB, sh, ea, mc, stream);
 }
 
 }  // namespace flce

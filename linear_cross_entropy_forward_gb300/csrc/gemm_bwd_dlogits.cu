@@ -14,12 +14,12 @@ cudaError_t launch_bwd_dlogits(const CUtensorMap& tmA, const CUtensorMap& tmB, c
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   int mc = max_clusters[dev].load();
   if (mc <= 0) {
-    e = pair_max_clusters<EPI_DLOGITS, false, true>(&mc);
+    e = pair_max_clusters<EPI_DLOGITS, false, true, TN_DLOGITS>(&mc);
     if (e != cudaSuccess) return e;
     if (mc <= 0) return cudaErrorInvalidConfiguration;
     max_clusters[dev].store(mc);
   }
-  return launch_gemm_pair<EPI_DLOGITS, false, true>(tmA, tmB, sh, ea, mc, stream);
+  return launch_gemm_pair<EPI_DLOGITS, false, true, TN_DLOGITS>(tmA, tmB, sh, ea, mc, stream);
 }
 
 }  // namespace flce
