@@ -28,7 +28,8 @@
  *   - All tensor pointers are DEVICE pointers to dense row-major arrays, owned by
  *     the caller; the library allocates no device memory and keeps no state
  *     between calls apart from a per-device cache of kernel attributes.
- *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns).
+ *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns); weight and
+ *     dweight are [H,V] or [V,H] as params->weight_layout says.
  *     labels: int64.  Everything else: fp32.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *     enqueued asynchronously on it; nothing synchronises unless params->validate
@@ -50,6 +51,15 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* Storage of weight (and of dweight, which always matches it).  WEIGHT_HV is the
+ * [H,V] matrix of the pages' logits = hidden @ weight (verl PR #462, "API");
+ * WEIGHT_VH is the transposed [V,H] layout of a torch nn.Linear LM head (the
+ * layout Liger-Kernel issue #127 works with), logits = hidden @ weight^T. */
+typedef enum {
+  FLCE_WEIGHT_HV = 0,
+  FLCE_WEIGHT_VH = 1
+} flce_weight_layout;
 
 typedef enum {
   FLCE_RED_NONE = 0,
@@ -80,6 +90,7 @@ typedef struct {
   float softcap;         /* tanh logit soft-cap c, 0 = off */
   int32_t validate;      /* != 0: synchronise at the end and report device errors */
   int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto */
+  int32_t weight_layout; /* flce_weight_layout: how weight and dweight are stored */
 } flce_params;
 
 /* Bytes of device workspace that flce_forward (phase 0) or flce_backward (phase 1)
@@ -88,7 +99,7 @@ typedef struct {
 size_t flce_workspace_size(const flce_params* params, int phase);
 
 /* Forward pass.
- *   hidden  [N,H] bf16, weight [H,V] bf16, labels [N] int64.
+ *   hidden  [N,H] bf16, weight [H,V] (or [V,H]) bf16, labels [N] int64.
  *   loss, entropy: [N] fp32 for FLCE_RED_NONE, [1] fp32 otherwise (overwritten).
  *   lse, ez: [N] fp32, per-row logsumexp and softmax mean E_p[z] of the capped
  *     logits, written for every row (ignored ones too); flce_backward needs them.
@@ -102,7 +113,7 @@ int flce_forward(const flce_params* params, const void* hidden, const void* weig
  *   lse, ez: the [N] outputs of flce_forward for the same inputs and params.
  *   g_loss, g_entropy: upstream gradients of loss and entropy, [N] for
  *     FLCE_RED_NONE, [1] otherwise; NULL means zero.
- *   dhidden [N,H] bf16, dweight [H,V] bf16: overwritten.
+ *   dhidden [N,H] bf16, dweight [H,V] (or [V,H], as weight) bf16: overwritten.
  *   workspace: >= flce_workspace_size(params, 1) bytes, 256-byte aligned. */
 int flce_backward(const flce_params* params, const void* hidden, const void* weight,
                   const int64_t* labels, const float* lse, const float* ez,

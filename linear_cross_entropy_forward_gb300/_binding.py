@@ -33,7 +33,20 @@ class FlceParams(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("H", ctypes.c_int64), ("V", ctypes.c_int64),
                 ("ignore_index", ctypes.c_int64), ("reduction", ctypes.c_int32),
                 ("zloss_coef", ctypes.c_float), ("softcap", ctypes.c_float),
-                ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64)]
+                ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64),
+                ("weight_layout", ctypes.c_int32)]
+
+
+WEIGHT_HV, WEIGHT_VH = 0, 1
+
+
+def layout_code(layout) -> int:
+    """'hv' (weight [H,V], the default) or 'vh' (weight [V,H], nn.Linear) -> ABI code."""
+    if layout in (WEIGHT_HV, "hv"):
+        return WEIGHT_HV
+    if layout in (WEIGHT_VH, "vh"):
+        return WEIGHT_VH
+    raise ValueError(f"weight_layout must be 'hv' or 'vh', got {layout!r}")
 
 
 _lib = None
@@ -80,9 +93,17 @@ def _check(code: int):
 
 
 def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
-                softcap=0.0, validate=False, chunk_v=0) -> FlceParams:
+                softcap=0.0, validate=False, chunk_v=0, weight_layout="hv") -> FlceParams:
     return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
-                      float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v))
+                      float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v),
+                      layout_code(weight_layout))
+
+
+def _dims(hidden, weight, weight_layout):
+    N, H = hidden.shape
+    V = weight.shape[1] if layout_code(weight_layout) == WEIGHT_HV else weight.shape[0]
+    wshape = (H, V) if layout_code(weight_layout) == WEIGHT_HV else (V, H)
+    return N, H, V, wshape
 
 
 def workspace_size(params: FlceParams, phase: int) -> int:
@@ -126,19 +147,20 @@ def _workspace(params, phase, device, workspace):
 
 def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
                  zloss_coef=0.0, softcap=0.0, validate=False, workspace=None, stream=None,
-                 out=None):
+                 out=None, weight_layout="hv"):
     """Forward pass through the C ABI.
 
     Returns (loss, entropy, lse, ez): loss/entropy are [N] for reduction 'none'
     and [1] otherwise; lse/ez are the per-row [N] statistics saved for backward.
+    weight is [H,V] (weight_layout 'hv') or [V,H] ('vh', nn.Linear).
     """
     lib = load_library()
-    N, H = hidden.shape
-    V = weight.shape[1]
+    N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, (H, V))
+    _need(weight, "weight", torch.bfloat16, wshape)
     _need(labels, "labels", torch.int64, (N,))
-    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate)
+    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
+                    weight_layout=weight_layout)
     dev = hidden.device
     n_out = N if p.reduction == RED_NONE else 1
     if out is None:
@@ -157,20 +179,21 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
 
 def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
                   ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, validate=False,
-                  chunk_v=0, workspace=None, stream=None, out=None):
-    """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight [H,V] bf16).
+                  chunk_v=0, workspace=None, stream=None, out=None, weight_layout="hv"):
+    """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight bf16 shaped
+    like weight).
 
     g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
     """
     lib = load_library()
-    N, H = hidden.shape
-    V = weight.shape[1]
+    N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, (H, V))
+    _need(weight, "weight", torch.bfloat16, wshape)
     _need(labels, "labels", torch.int64, (N,))
     _need(lse, "lse", torch.float32, (N,))
     _need(ez, "ez", torch.float32, (N,))
-    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v)
+    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v,
+                    weight_layout)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
         _need(g_loss, "g_loss", torch.float32, (n_g,))
@@ -179,7 +202,7 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     dev = hidden.device
     if out is None:
         dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
-        dw = torch.empty(H, V, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
     else:
         dh, dw = out
     ws = _workspace(p, 1, dev, workspace)
@@ -196,11 +219,12 @@ def flce_status(workspace, stream=None) -> int:
 
 class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap):
+    def forward(ctx, hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap,
+                weight_layout):
         loss, ent, lse, ez = flce_forward(hidden, weight, labels, reduction, ignore_index,
-                                          zloss_coef, softcap)
+                                          zloss_coef, softcap, weight_layout=weight_layout)
         ctx.save_for_backward(hidden, weight, labels, lse, ez)
-        ctx.cfg = (reduction, ignore_index, zloss_coef, softcap)
+        ctx.cfg = (reduction, ignore_index, zloss_coef, softcap, weight_layout)
         if reduction_code(reduction) != RED_NONE:
             loss, ent = loss[0], ent[0]
         return loss, ent
@@ -208,7 +232,7 @@ class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g_loss, g_ent):
         hidden, weight, labels, lse, ez = ctx.saved_tensors
-        reduction, ignore_index, zloss_coef, softcap = ctx.cfg
+        reduction, ignore_index, zloss_coef, softcap, weight_layout = ctx.cfg
         n_g = hidden.shape[0] if reduction_code(reduction) == RED_NONE else 1
 
         def prep(g):
@@ -217,18 +241,19 @@ class _LinearCrossEntropy(torch.autograd.Function):
             return g.detach().reshape(n_g).to(torch.float32).contiguous()
 
         dh, dw = flce_backward(hidden, weight, labels, lse, ez, prep(g_loss), prep(g_ent),
-                               reduction, ignore_index, zloss_coef, softcap)
-        return dh, dw, None, None, None, None, None
+                               reduction, ignore_index, zloss_coef, softcap,
+                               weight_layout=weight_layout)
+        return dh, dw, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
-                         zloss_coef=0.0, softcap=0.0):
+                         zloss_coef=0.0, softcap=0.0, weight_layout="hv"):
     """loss, entropy = linear_cross_entropy(hidden, weight, labels, reduction)
 
     The call of verl PR #462 ("API"): hidden [N,H] bf16, weight [H,V] bf16,
     labels [N] int64.  `loss` is the cross-entropy (+ z-loss); the page's
     log-probability is -loss when z-loss is off.  Differentiable w.r.t. hidden
-    and weight.
+    and weight.  weight_layout='vh' takes an nn.Linear-style weight [V,H].
     """
     return _LinearCrossEntropy.apply(hidden, weight, labels, reduction, ignore_index,
-                                     zloss_coef, softcap)
+                                     zloss_coef, softcap, weight_layout)

@@ -24,16 +24,6 @@
 
 namespace flce {
 
-// GEMM launchers (gemm_*.cu): CTA-pair kernels on 256 x TN tiles.
-cudaError_t launch_fwd_stats(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                             const EpiArgs&, cudaStream_t);
-cudaError_t launch_bwd_dlogits(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, cudaStream_t);
-cudaError_t launch_bwd_dweight(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, cudaStream_t);
-cudaError_t launch_bwd_dhidden(const CUtensorMap&, const CUtensorMap&, const GemmShape&,
-                               const EpiArgs&, cudaStream_t);
-
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
@@ -237,6 +227,8 @@ int check_params(const flce_params* p) {
   if (p->N > kMaxDim || p->H > kMaxDim || p->V > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   if (p->H % 8 != 0 || p->V % 8 != 0) return FLCE_ERR_ALIGN;
   if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % 256 != 0)) return FLCE_ERR_BAD_ARG;
+  if (p->weight_layout != FLCE_WEIGHT_HV && p->weight_layout != FLCE_WEIGHT_VH)
+    return FLCE_ERR_BAD_ARG;
   // chunk-relative and vocabulary column indices are 32-bit inside the kernels
   if (cdiv(p->V, 256) * 256 > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   return FLCE_OK;
@@ -420,9 +412,13 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
     return p->validate ? read_status(ws, st) : FLCE_OK;
   }
 
+  const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, hidden, H, N, H, BK, 128)) return FLCE_ERR_CUDA;
-  if (!make_map(&tmB, weight, V, H, V, 64, BK)) return FLCE_ERR_CUDA;
+  // weight as B: [H,V] is MN-major ({64,64} boxes), [V,H] K-major ({64, TN/2} boxes)
+  if (!(vh ? make_map(&tmB, weight, H, V, H, BK, TN_FWD / 2)
+           : make_map(&tmB, weight, V, H, V, 64, BK)))
+    return FLCE_ERR_CUDA;
   // hidden is revisited by every vocabulary tile of its group; the weight streams
   GemmShape sh = base_shape(L2_EVICT_LAST, L2_NORMAL);
   sh.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
@@ -444,7 +440,8 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   ea.part_stride = N;
   ea.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
   ea.err = err;
-  if ((rc = cuda_rc(launch_fwd_stats(tmA, tmB, sh, ea, st)))) return rc;
+  if ((rc = cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st))))
+    return rc;
 
   float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
   float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
@@ -498,12 +495,21 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
                                       p->reduction == FLCE_RED_MEAN, p->zloss_coef, rowc);
   if ((rc = cuda_rc(cudaGetLastError()))) return rc;
 
-  CUtensorMap mHidK, mWMn, mHidMn, mDlMn, mDlK, mWK;
-  bool ok = make_map(&mHidK, hidden, H, N, H, BK, 128) && make_map(&mWMn, weight, V, H, V, 64, BK) &&
+  // Operand tensor maps.  hidden: K-major (recompute) and MN-major (dweight);
+  // dlogits chunk: MN-major (dweight) and K-major (dhidden); weight: as the
+  // recompute's B and as dhidden's B, each K- or MN-major depending on its layout.
+  const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
+  CUtensorMap mHidK, mHidMn, mDlMn, mDlK, mWRec, mWDh;
+  bool ok = make_map(&mHidK, hidden, H, N, H, BK, 128) &&
             make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
             make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
-            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, 128) &&
-            make_map(&mWK, weight, V, H, V, BK, TN_DHIDDEN / 2);
+            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, 128);
+  if (vh)
+    ok = ok && make_map(&mWRec, weight, H, V, H, BK, TN_DLOGITS / 2) &&
+         make_map(&mWDh, weight, H, V, H, 64, BK);
+  else
+    ok = ok && make_map(&mWRec, weight, V, H, V, 64, BK) &&
+         make_map(&mWDh, weight, V, H, V, BK, TN_DHIDDEN / 2);
   if (!ok) return FLCE_ERR_CUDA;
 
   for (int64_t c = 0; c < L.chunks; ++c) {
@@ -530,25 +536,42 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e3.dl = dl;
     e3.ld_dl = L.Vc;
     e3.err = err;
-    if ((rc = cuda_rc(launch_bwd_dlogits(mHidK, mWMn, s3, e3, st)))) return rc;
+    if ((rc = cuda_rc((vh ? launch_bwd_dlogits_vh : launch_bwd_dlogits)(mHidK, mWRec, s3, e3,
+                                                                        st))))
+      return rc;
 
-    // dweight[:, v0:v0+w] = hidden^T @ dlogits
-    // hidden^T revisited by every column tile of the chunk; dlogits streamed
-    GemmShape s4 = base_shape(L2_EVICT_LAST, L2_NORMAL);
-    s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
-    s4.n_tiles = static_cast<int>(cdiv(w, TN_DWEIGHT));
+    // dweight for the chunk, written once: [H,V] -> dweight[:, v0:v0+w] = hidden^T @ dlogits
+    // (rows h, hidden^T revisited); [V,H] -> dweight[v0:v0+w, :] = dlogits^T @ hidden
+    // (rows v, hidden revisited as B).  Both operands are MN-major views.
+    GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
-    s4.raster = 0;
-    s4.group = raster_group(int64_t(PAIR_BM) * N * 2, s4.m_tiles);
     EpiArgs e4{};
-    e4.rows = static_cast<int>(H);
-    e4.cols = static_cast<int>(w);
-    e4.col_base = static_cast<int>(v0);
     e4.V = V;
-    e4.out = static_cast<__nv_bfloat16*>(dweight);
-    e4.ld_out = V;
     e4.err = err;
-    if ((rc = cuda_rc(launch_bwd_dweight(mHidMn, mDlMn, s4, e4, st)))) return rc;
+    e4.col_base = 0;
+    if (vh) {
+      s4.m_tiles = static_cast<int>(cdiv(w, PAIR_BM));
+      s4.n_tiles = static_cast<int>(cdiv(H, TN_DWEIGHT));
+      s4.raster = 1;
+      s4.group = raster_group(int64_t(TN_DWEIGHT) * N * 2, s4.n_tiles);
+      e4.rows = static_cast<int>(w);
+      e4.cols = static_cast<int>(H);
+      e4.out = static_cast<__nv_bfloat16*>(dweight) + v0 * H;
+      e4.ld_out = H;
+    } else {
+      s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
+      s4.n_tiles = static_cast<int>(cdiv(w, TN_DWEIGHT));
+      s4.raster = 0;
+      s4.group = raster_group(int64_t(PAIR_BM) * N * 2, s4.m_tiles);
+      e4.rows = static_cast<int>(H);
+      e4.cols = static_cast<int>(w);
+      e4.col_base = static_cast<int>(v0);
+      e4.out = static_cast<__nv_bfloat16*>(dweight);
+      e4.ld_out = V;
+    }
+    if ((rc = cuda_rc(vh ? launch_bwd_dweight(mDlMn, mHidMn, s4, e4, st)
+                         : launch_bwd_dweight(mHidMn, mDlMn, s4, e4, st))))
+      return rc;
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
     // the weight chunk is revisited by every row tile; dlogits rows streamed
@@ -571,7 +594,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
                   : c == L.chunks - 1 ? ACC_LAST
                                       : ACC_MID;
     e5.err = err;
-    if ((rc = cuda_rc(launch_bwd_dhidden(mDlK, mWK, s5, e5, st)))) return rc;
+    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK, mWDh, s5, e5,
+                                                                        st))))
+      return rc;
   }
   return p->validate ? read_status(ws, st) : FLCE_OK;
 }

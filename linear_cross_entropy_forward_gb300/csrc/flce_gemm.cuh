@@ -26,6 +26,8 @@
 // {64, rows}; MN-major tiles as rows/64 boxes {64, 64} stacked 8 KB apart.
 #pragma once
 
+#include <atomic>
+
 #include "flce_device.cuh"
 
 namespace flce {
@@ -577,5 +579,44 @@ cudaError_t pair_max_clusters(int* out) {
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
 }
+
+// Launch with the co-resident pair count of this instantiation, queried once per
+// device (the query needs the kernel's attributes set, so it is cached here).
+template <int EPI, bool A_MN, bool B_MN, int TN>
+cudaError_t launch_pair_cached(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                               const GemmShape& sh, const EpiArgs& ea, cudaStream_t stream) {
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int mc = max_clusters[dev].load();
+  if (mc <= 0) {
+    e = pair_max_clusters<EPI, A_MN, B_MN, TN>(&mc);
+    if (e != cudaSuccess) return e;
+    if (mc <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters[dev].store(mc);
+  }
+  return launch_gemm_pair<EPI, A_MN, B_MN, TN>(tmA, tmB, sh, ea, mc, stream);
+}
+
+// Launchers of the instantiations the path uses (one translation unit each).
+#define FLCE_DECLARE_LAUNCHER(name)                                                  \
+  cudaError_t name(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh, \
+                   const EpiArgs& ea, cudaStream_t stream)
+#define FLCE_DEFINE_LAUNCHER(name, EPI, A_MN, B_MN, TN)                                  \
+  FLCE_DECLARE_LAUNCHER(name) {                                                          \
+    return launch_pair_cached<EPI, A_MN, B_MN, TN>(tmA, tmB, sh, ea, stream);           \
+  }
+
+// weight stored [H, V]
+FLCE_DECLARE_LAUNCHER(launch_fwd_stats);     // hidden (K) x weight (MN)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dlogits);   // hidden (K) x weight (MN)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dweight);   // hidden^T (MN) x dlogits (MN); also dlogits^T (MN) x hidden (MN)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dhidden);   // dlogits (K) x weight (K)
+// weight stored [V, H] (the nn.Linear layout)
+FLCE_DECLARE_LAUNCHER(launch_fwd_stats_vh);    // hidden (K) x weight (K)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dlogits_vh);  // hidden (K) x weight (K)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dhidden_vh);  // dlogits (K) x weight (MN)
 
 }  // namespace flce

@@ -1,25 +1,6 @@
-// Instantiation: dhidden += dlogits @ weight_chunk^T (A = dlogits K-major, B = weight K-major).
-#include <atomic>
-
+// Instantiation: dhidden += dlogits x weight chunk; dlogits K-major, weight [H,V] K-major.
 #include "flce_gemm.cuh"
 
 namespace flce {
-
-cudaError_t launch_bwd_dhidden(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh,
-                           const EpiArgs& ea, cudaStream_t stream) {
-  static std::atomic<int> max_clusters[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int mc = max_clusters[dev].load();
-  if (mc <= 0) {
-    e = pair_max_clusters<EPI_ACCUM, false, false, TN_DHIDDEN>(&mc);
-    if (e != cudaSuccess) return e;
-    if (mc <= 0) return cudaErrorInvalidConfiguration;
-    max_clusters[dev].store(mc);
-  }
-  return launch_gemm_pair<EPI_ACCUM, false, false, TN_DHIDDEN>(tmA, tmB, sh, ea, mc, stream);
-}
-
+FLCE_DEFINE_LAUNCHER(launch_bwd_dhidden, EPI_ACCUM, false, false, TN_DHIDDEN)
 }  // namespace flce

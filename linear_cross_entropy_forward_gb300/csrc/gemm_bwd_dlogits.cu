@@ -1,25 +1,6 @@
-// Instantiation: backward recompute -> dlogits chunk (A = hidden K-major, B = weight MN-major).
-#include <atomic>
-
+// Instantiation: backward recompute -> dlogits chunk; hidden K-major, weight [H,V] MN-major.
 #include "flce_gemm.cuh"
 
 namespace flce {
-
-cudaError_t launch_bwd_dlogits(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh,
-                           const EpiArgs& ea, cudaStream_t stream) {
-  static std::atomic<int> max_clusters[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int mc = max_clusters[dev].load();
-  if (mc <= 0) {
-    e = pair_max_clusters<EPI_DLOGITS, false, true, TN_DLOGITS>(&mc);
-    if (e != cudaSuccess) return e;
-    if (mc <= 0) return cudaErrorInvalidConfiguration;
-    max_clusters[dev].store(mc);
-  }
-  return launch_gemm_pair<EPI_DLOGITS, false, true, TN_DLOGITS>(tmA, tmB, sh, ea, mc, stream);
-}
-
+FLCE_DEFINE_LAUNCHER(launch_bwd_dlogits, EPI_DLOGITS, false, true, TN_DLOGITS)
 }  // namespace flce

@@ -42,9 +42,10 @@ def test_version_and_strerror(lib):
 
 
 def test_params_struct_layout():
-    # int64 x4, int32, float, float, int32, int64 -> 56 bytes, as in flce.h
-    assert ctypes.sizeof(B.FlceParams) == 56
+    # int64 x4, int32, float, float, int32, int64, int32 (+4 padding) -> 64 bytes, as in flce.h
+    assert ctypes.sizeof(B.FlceParams) == 64
     assert B.FlceParams.chunk_v.offset == 48
+    assert B.FlceParams.weight_layout.offset == 56
 
 
 def test_workspace_sizes(lib):
@@ -70,12 +71,16 @@ def test_workspace_sizes(lib):
     (dict(N=10, H=64, V=0), 2),
     (dict(N=10, H=64, V=64, chunk_v=100), 1),
     (dict(N=10, H=64, V=64, zloss_coef=-1.0), 1),
+    (dict(N=10, H=64, V=64, weight_layout=7), 1),
 ])
 def test_bad_params_rejected_on_host(lib, kw, code):
     args = dict(N=10, H=64, V=64)
     args.update(kw)
     red = args.pop("reduction", "mean")
+    bad_layout = args.pop("weight_layout", None)
     p = flce.make_params(args.pop("N"), args.pop("H"), args.pop("V"), red, **args)
+    if bad_layout is not None:
+        p.weight_layout = bad_layout
     assert lib.flce_workspace_size(ctypes.byref(p), 0) == 0
     fake = ctypes.c_void_p(0x1000)
     rc = lib.flce_forward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, fake,

@@ -47,24 +47,29 @@ def oracle_run(w, hidden, weight, labels, g_loss, g_ent):
     return o, dh, dw
 
 
-def gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v=0):
+def gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v=0, weight_layout="hv"):
+    """weight is [H,V]; with weight_layout 'vh' the GPU gets its [V,H] transpose and the
+    returned dw is transposed back to [H,V]."""
     dev = torch.device("cuda")
-    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
-    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, zloss_coef=w.zloss_coef,
-                                      softcap=w.softcap, validate=True)
+    hd, yd = hidden.to(dev), labels.to(dev)
+    Wd = weight.to(dev) if weight_layout == "hv" else weight.t().contiguous().to(dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=weight_layout)
+    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True, **kw)
     dh, dw = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
-                           zloss_coef=w.zloss_coef, softcap=w.softcap, validate=True,
-                           chunk_v=chunk_v)
+                           validate=True, chunk_v=chunk_v, **kw)
     torch.cuda.synchronize()
+    if weight_layout == "vh":
+        assert dw.shape == (w.V, w.H)
+        dw = dw.t()
     f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
     return dict(loss=f(loss), entropy=f(ent), lse=f(lse), ez=f(ez), dh=f(dh), dw=f(dw),
                 dh_raw=dh.cpu())
 
 
-def check_parity(w, chunk_v=0, report=None):
+def check_parity(w, chunk_v=0, report=None, weight_layout="hv"):
     hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
     o, dh_o, dw_o = oracle_run(w, hidden, weight, labels, g_loss, g_ent)
-    g = gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v)
+    g = gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v, weight_layout)
     valid = o["valid"]
     errs = {}
     errs["lse_abs"] = float(np.abs(g["lse"] - o["lse"]).max())
@@ -131,6 +136,32 @@ def test_parity_small(name, w, chunk_v):
     rep = {}
     check_parity(w, chunk_v, rep)
     print(name, rep)
+
+
+VH_CASES = [c for c in CASES if c[0] in ("tiny", "ragged_none", "ragged_mean_zloss",
+                                          "softcap_tight", "single_tile", "one_row")]
+
+
+@pytest.mark.parametrize("name,w,chunk_v", VH_CASES, ids=[c[0] for c in VH_CASES])
+def test_parity_weight_vh(name, w, chunk_v):
+    """Weight stored [V,H] (nn.Linear layout): same results as the [H,V] oracle."""
+    _cuda_or_skip()
+    rep = {}
+    check_parity(w, chunk_v, rep, weight_layout="vh")
+    print(name, "vh", rep)
+
+
+def test_layouts_agree_bitwise():
+    """The two weight layouts run kernels with different operand-major descriptors,
+    but the UMMAs sum the same products in the same K order: identical results."""
+    _cuda_or_skip()
+    w = dataclasses.replace(W0, name="lay", N=300, H=200, V=1000, zloss_coef=1e-3,
+                            softcap=5.0)
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    a = gpu_run(w, hidden, weight, labels, g_loss, g_ent, 256, "hv")
+    b = gpu_run(w, hidden, weight, labels, g_loss, g_ent, 256, "vh")
+    for k in ("loss", "entropy", "lse", "ez", "dh", "dw"):
+        assert np.array_equal(a[k], b[k]), k
 
 
 def test_all_ignored_mean_is_zero():
