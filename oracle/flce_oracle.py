@@ -19,11 +19,21 @@ What it computes (plain definitions, written out in fp64):
   applied to the logits after the matmul in three steps (divide by c, tanh,
   multiply by c); its backward follows from the chain rule, d tanh(x)/dx =
   1 - tanh(x)^2.
+* Liger-Kernel PR #551 (review): label smoothing and per-class target weights
+  are further options of the same loss.  Their definition here is torch's
+  cross_entropy(weight=w, label_smoothing=eps): the cross-entropy part of a
+  token is (1 - eps) w_y (lse - z_y) + (eps / V) sum_c w_c (lse - z_c), and the
+  mean divides it by the sum of w_y over non-ignored tokens.  The z-loss and the
+  entropy stay unweighted and their mean divides by the non-ignored count
+  (the review asks for n_non_ignore in the entropy term).
 
 Backward (closed form of the derivative of the objective
 J = sum_n gl_n * loss_n + ge_n * entropy_n, with gl/ge the upstream gradients
-after the reduction's scaling and zero on ignored rows):
+after the reduction's scaling and zero on ignored rows; without smoothing and
+weights):
     dz_nv = gl_n * (p_nv - [v == y_n] + 2 coef lse_n p_nv) - ge_n * p_nv * (z_nv - E_p[z]_n)
+With smoothing eps and class weights w (W = sum_c w_c), the cross-entropy part
+contributes a_n (p_nv ((1 - eps) w_y + eps W / V) - (1 - eps) w_y [v == y_n] - eps w_v / V).
     dz'_nv = dz_nv * (1 - (z_nv / c)^2)            (soft-cap on)
     dhidden = dz' @ weight^T,   dweight = hidden^T @ dz'
 
@@ -57,6 +67,15 @@ def _cap(zp: np.ndarray, softcap: float) -> np.ndarray:
     return softcap * np.tanh(zp / softcap)
 
 
+def _class_weights(class_weight, V):
+    if class_weight is None:
+        return np.ones(V)
+    w = np.asarray(class_weight, dtype=np.float64).reshape(-1)
+    if w.shape != (V,):
+        raise ValueError("class_weight must have V entries")
+    return w
+
+
 def _check(hidden, weight, labels, reduction, ignore_index):
     if reduction not in _REDS:
         raise ValueError(f"reduction must be one of {_REDS}")
@@ -77,11 +96,12 @@ def logits_chunk(hidden: np.ndarray, weight: np.ndarray, v0: int, v1: int,
     return _cap(hidden @ weight[:, v0:v1], softcap)
 
 
-def row_stats(hidden, weight, softcap=0.0, v_chunk=8192):
-    """Per-row log-sum-exp and softmax mean of the capped logits.
+def row_stats(hidden, weight, softcap=0.0, v_chunk=8192, class_weight=None):
+    """Per-row log-sum-exp, softmax mean and class-weighted sum of the capped logits.
 
     Pass 1: m_n = max_v z_nv.  Pass 2: d_n = sum_v exp(z_nv - m_n) and
     s_n = sum_v exp(z_nv - m_n) * z_nv.  Then lse = m + log d, E_p[z] = s / d.
+    Also sw_n = sum_v w_v z_nv (w = class_weight, ones by default).
     """
     N = hidden.shape[0]
     V = weight.shape[1]
@@ -89,16 +109,20 @@ def row_stats(hidden, weight, softcap=0.0, v_chunk=8192):
     for v0 in range(0, V, v_chunk):
         z = logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap)
         m = np.maximum(m, z.max(axis=1))
+    cw = _class_weights(class_weight, V)
     d = np.zeros(N)
     s = np.zeros(N)
+    sw = np.zeros(N)
     for v0 in range(0, V, v_chunk):
-        z = logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap)
+        v1 = min(V, v0 + v_chunk)
+        z = logits_chunk(hidden, weight, v0, v1, softcap)
         e = np.exp(z - m[:, None])
         d += e.sum(axis=1)
         s += (e * z).sum(axis=1)
+        sw += z @ cw[v0:v1]
     lse = m + np.log(d)
     ez = s / d
-    return lse, ez
+    return lse, ez, sw
 
 
 def label_logits(hidden, weight, labels, valid, softcap=0.0):
@@ -112,7 +136,7 @@ def label_logits(hidden, weight, labels, valid, softcap=0.0):
 
 
 def forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
-            zloss_coef=0.0, softcap=0.0, v_chunk=8192):
+            zloss_coef=0.0, softcap=0.0, v_chunk=8192, label_smoothing=0.0, class_weight=None):
     """Loss and entropy of verl PR #462's compute logic, with the Liger options.
 
     Returns a dict:
@@ -125,49 +149,69 @@ def forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
     hidden = np.asarray(hidden, dtype=np.float64)
     weight = np.asarray(weight, dtype=np.float64)
     N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
-    lse, ez = row_stats(hidden, weight, softcap, v_chunk)
+    cw = _class_weights(class_weight, V)
+    eps = float(label_smoothing)
+    lse, ez, sw = row_stats(hidden, weight, softcap, v_chunk, class_weight)
     zy = label_logits(hidden, weight, lab, valid, softcap)
-    ce = np.where(valid, lse - zy, 0.0)
+    wy = np.where(valid, cw[np.where(valid, lab, 0)], 0.0)
+    # cross-entropy part: (1 - eps) w_y (lse - z_y) + eps/V (W lse - sum_c w_c z_c)
+    ce = np.where(valid, (1.0 - eps) * wy * (lse - zy) + (eps / V) * (cw.sum() * lse - sw), 0.0)
     ent = np.where(valid, lse - ez, 0.0)
     zl = np.where(valid, zloss_coef * lse * lse, 0.0)
     loss_tok = ce + zl
     n_valid = int(valid.sum())
+    w_valid = float(wy.sum())
     if reduction == "none":
         loss, entropy = loss_tok, ent
     elif reduction == "sum":
         loss, entropy = float(loss_tok.sum()), float(ent.sum())
     else:
-        # mean over non-ignored tokens; an all-ignored batch reduces to 0
-        den = float(n_valid) if n_valid > 0 else None
-        loss = float(loss_tok.sum()) / den if den else 0.0
-        entropy = float(ent.sum()) / den if den else 0.0
+        # mean over non-ignored tokens (the cross-entropy part over their summed class
+        # weights); an all-ignored batch reduces to 0
+        loss = (float(ce.sum()) / w_valid if w_valid != 0 else 0.0) + \
+            (float(zl.sum()) / n_valid if n_valid > 0 else 0.0)
+        entropy = float(ent.sum()) / n_valid if n_valid > 0 else 0.0
     return dict(loss=loss, entropy=entropy, loss_tok=loss_tok, entropy_tok=ent, ce_tok=ce,
-                lse=lse, ez=ez, n_valid=n_valid, valid=valid)
+                lse=lse, ez=ez, n_valid=n_valid, valid=valid, w_valid=w_valid)
 
 
-def grad_scales(g_loss, g_entropy, valid, reduction):
-    """Per-row upstream gradients after the reduction: g (none/sum) or g / n_valid (mean),
-    zero on ignored rows."""
+def grad_scales(g_loss, g_entropy, valid, reduction, w_valid=None):
+    """Per-row upstream gradients after the reduction, zero on ignored rows:
+    (gl_ce, gl_z, ge) = g (none/sum); for mean the cross-entropy part's is divided
+    by the summed class weights w_valid (the non-ignored count without weights),
+    the z-loss and entropy parts' by the non-ignored count."""
     N = valid.shape[0]
     gl = np.broadcast_to(np.asarray(g_loss, dtype=np.float64).reshape(-1), (N,)).copy()
     ge = np.broadcast_to(np.asarray(g_entropy, dtype=np.float64).reshape(-1), (N,)).copy()
+    gc = gl.copy()
     if reduction == "mean":
         n_valid = int(valid.sum())
         s = 1.0 / n_valid if n_valid > 0 else 0.0
+        wv = float(n_valid) if w_valid is None else float(w_valid)
+        gc *= 1.0 / wv if wv != 0 else 0.0
         gl *= s
         ge *= s
+    gc[~valid] = 0.0
     gl[~valid] = 0.0
     ge[~valid] = 0.0
-    return gl, ge
+    return gc, gl, ge
 
 
-def dlogits_chunk(hidden, weight, labels, lse, ez, gl, ge, v0, v1,
-                  zloss_coef=0.0, softcap=0.0):
-    """Gradient of the objective w.r.t. the raw (pre-cap) logits z'[:, v0:v1]."""
+def dlogits_chunk(hidden, weight, labels, lse, ez, gc, gl, ge, v0, v1,
+                  zloss_coef=0.0, softcap=0.0, label_smoothing=0.0, class_weight=None):
+    """Gradient of the objective w.r.t. the raw (pre-cap) logits z'[:, v0:v1]
+    (gc, gl, ge: per-row scaled upstream grads of the cross-entropy part, the
+    z-loss part and the entropy, from grad_scales)."""
+    V = weight.shape[1]
+    cw = _class_weights(class_weight, V)
+    eps = float(label_smoothing)
     z = logits_chunk(hidden, weight, v0, v1, softcap)
     p = np.exp(z - lse[:, None])
     onehot = (labels[:, None] == np.arange(v0, v1)[None, :]).astype(np.float64)
-    dz = gl[:, None] * (p - onehot + 2.0 * zloss_coef * lse[:, None] * p) \
+    wy = cw[np.clip(labels, 0, V - 1)][:, None]
+    ce_grad = p * ((1.0 - eps) * wy + eps * cw.sum() / V) - (1.0 - eps) * wy * onehot \
+        - (eps / V) * cw[v0:v1][None, :]
+    dz = gc[:, None] * ce_grad + gl[:, None] * 2.0 * zloss_coef * lse[:, None] * p \
         - ge[:, None] * p * (z - ez[:, None])
     if softcap != 0.0:
         dz = dz * (1.0 - (z / softcap) ** 2)
@@ -176,7 +220,7 @@ def dlogits_chunk(hidden, weight, labels, lse, ez, gl, ge, v0, v1,
 
 def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, v_chunk=8192,
-             rows=None):
+             rows=None, label_smoothing=0.0, class_weight=None):
     """(dhidden, dweight) in fp64.
 
     ``lse``/``ez`` must come from :func:`forward` on the same inputs.  With
@@ -186,32 +230,38 @@ def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean
     hidden = np.asarray(hidden, dtype=np.float64)
     weight = np.asarray(weight, dtype=np.float64)
     N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
-    gl, ge = grad_scales(g_loss, g_entropy, valid, reduction)
+    cw = _class_weights(class_weight, V)
+    w_valid = float(np.where(valid, cw[np.where(valid, lab, 0)], 0.0).sum())
+    gc, gl, ge = grad_scales(g_loss, g_entropy, valid, reduction, w_valid)
+    opts = dict(zloss_coef=zloss_coef, softcap=softcap, label_smoothing=label_smoothing,
+                class_weight=class_weight)
     if rows is not None:
         rows = np.asarray(rows, dtype=np.int64)
         hs, ls, vs = hidden[rows], lab[rows], valid[rows]
         dh = np.zeros((rows.size, H))
         for v0 in range(0, V, v_chunk):
             v1 = min(V, v0 + v_chunk)
-            dz = dlogits_chunk(hs, weight, ls, lse[rows], ez[rows], gl[rows], ge[rows], v0, v1,
-                               zloss_coef, softcap)
+            dz = dlogits_chunk(hs, weight, ls, lse[rows], ez[rows], gc[rows], gl[rows], ge[rows],
+                               v0, v1, **opts)
             dh += dz @ weight[:, v0:v1].T
         return dh, None
     dh = np.zeros((N, H))
     dw = np.zeros((H, V))
     for v0 in range(0, V, v_chunk):
         v1 = min(V, v0 + v_chunk)
-        dz = dlogits_chunk(hidden, weight, lab, lse, ez, gl, ge, v0, v1, zloss_coef, softcap)
+        dz = dlogits_chunk(hidden, weight, lab, lse, ez, gc, gl, ge, v0, v1, **opts)
         dh += dz @ weight[:, v0:v1].T
         dw[:, v0:v1] = hidden.T @ dz
     return dh, dw
 
 
 def objective(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
-              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0):
+              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, label_smoothing=0.0,
+              class_weight=None):
     """J = <g_loss, loss> + <g_entropy, entropy> (scalar), the function whose gradient
     :func:`backward` returns.  Used for finite-difference pins."""
-    out = forward(hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap)
+    out = forward(hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap,
+                  label_smoothing=label_smoothing, class_weight=class_weight)
     gl = np.asarray(g_loss, dtype=np.float64).reshape(-1)
     ge = np.asarray(g_entropy, dtype=np.float64).reshape(-1)
     if reduction == "none":

@@ -15,13 +15,20 @@ IGNORE_INDEX = -100
 
 
 def forward_loops(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
-                  zloss_coef=0.0, softcap=0.0):
-    """hidden: list of N lists of H floats; weight: H lists of V floats; labels: N ints."""
+                  zloss_coef=0.0, softcap=0.0, label_smoothing=0.0, class_weight=None):
+    """hidden: list of N lists of H floats; weight: H lists of V floats; labels: N ints.
+
+    With label smoothing eps and class weights w (torch's cross_entropy definition):
+    the cross-entropy of a token is (1 - eps) w_y (-log p_y) + eps/V sum_c w_c (-log p_c),
+    and the mean divides it by the summed w_y of the non-ignored tokens."""
     N = len(hidden)
     H = len(weight)
     V = len(weight[0])
-    loss_tok, ent_tok, lse_all = [], [], []
+    w = class_weight if class_weight is not None else [1.0] * V
+    eps = label_smoothing
+    ce_tok, zl_tok, loss_tok, ent_tok, lse_all = [], [], [], [], []
     n_valid = 0
+    w_valid = 0.0
     for n in range(N):
         z = []
         for v in range(V):
@@ -40,22 +47,30 @@ def forward_loops(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_
         lse_all.append(lse)
         y = labels[n]
         if y == ignore_index:
+            ce_tok.append(0.0)
+            zl_tok.append(0.0)
             loss_tok.append(0.0)
             ent_tok.append(0.0)
             continue
         n_valid += 1
-        ce = -math.log(p[y])
-        loss_tok.append(ce + zloss_coef * lse * lse)
+        w_valid += w[y]
+        smooth = 0.0
+        for c in range(V):
+            smooth += w[c] * -math.log(p[c])
+        ce = (1.0 - eps) * w[y] * -math.log(p[y]) + eps / V * smooth
+        zl = zloss_coef * lse * lse
+        ce_tok.append(ce)
+        zl_tok.append(zl)
+        loss_tok.append(ce + zl)
         ent_tok.append(ent)
     if reduction == "none":
         return loss_tok, ent_tok, lse_all
-    s_l = sum(loss_tok)
-    s_e = sum(ent_tok)
     if reduction == "sum":
-        return s_l, s_e, lse_all
-    if n_valid == 0:
-        return 0.0, 0.0, lse_all
-    return s_l / n_valid, s_e / n_valid, lse_all
+        return sum(loss_tok), sum(ent_tok), lse_all
+    loss = (sum(ce_tok) / w_valid if w_valid != 0 else 0.0) + \
+        (sum(zl_tok) / n_valid if n_valid else 0.0)
+    ent_mean = sum(ent_tok) / n_valid if n_valid else 0.0
+    return loss, ent_mean, lse_all
 
 
 def objective_loops(hidden, weight, labels, g_loss, g_entropy, reduction="mean",

@@ -231,9 +231,9 @@ def test_dlogit_rows_sum(cap):
     for zc in (0.0, 0.02):
         out = orc.forward(hidden, weight, labels, "none", zloss_coef=zc)
         gl, ge = _grads("none", 15, 12)
-        gls, ges = orc.grad_scales(gl, ge, out["valid"], "none")
-        dz = orc.dlogits_chunk(hidden, weight, labels, out["lse"], out["ez"], gls, ges, 0, 64,
-                               zloss_coef=zc)
+        gcs, gls, ges = orc.grad_scales(gl, ge, out["valid"], "none")
+        dz = orc.dlogits_chunk(hidden, weight, labels, out["lse"], out["ez"], gcs, gls, ges, 0,
+                               64, zloss_coef=zc)
         np.testing.assert_allclose(dz.sum(axis=1), 2 * zc * out["lse"] * gls, atol=1e-12)
         if cap == 0.0 and zc == 0.0:
             _, dw = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, "none")
@@ -308,3 +308,78 @@ def test_oracle_matches_scalar_loops(reduction, zc, cap):
                                ge.tolist(), reduction=reduction, zloss_coef=zc, softcap=cap)
     np.testing.assert_allclose(dh, np.array(fh), rtol=1e-5, atol=1e-7)
     np.testing.assert_allclose(dw, np.array(fw), rtol=1e-5, atol=1e-7)
+
+
+# --------------------------------------------------------------------------- smoothing, weights
+@pytest.mark.parametrize("reduction", REDS)
+@pytest.mark.parametrize("eps", [0.0, 0.1])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_smoothing_and_class_weights_match_torch(reduction, eps, weighted):
+    """torch's cross_entropy(weight, label_smoothing, ignore_index) is the definition."""
+    hidden, weight, labels = _rand_case(41, 13, 257, 40, w_std=0.9, ignore=(0, 7, 8))
+    cw = np.random.default_rng(41).uniform(0.2, 2.0, 257) if weighted else None
+    out = orc.forward(hidden, weight, labels, reduction, v_chunk=50, label_smoothing=eps,
+                      class_weight=cw)
+    z = torch.from_numpy(hidden) @ torch.from_numpy(weight)
+    ref = torch.nn.functional.cross_entropy(
+        z, torch.from_numpy(labels), weight=None if cw is None else torch.from_numpy(cw),
+        ignore_index=-100, reduction=reduction, label_smoothing=eps)
+    np.testing.assert_allclose(out["loss"], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("reduction", REDS)
+def test_smoothing_weights_zloss_softcap_finite_differences(reduction):
+    N, H, V = 6, 5, 9
+    hidden, weight, labels = _rand_case(N, H, V, 50, w_std=0.7, ignore=(2,))
+    cw = np.random.default_rng(50).uniform(0.3, 1.7, V)
+    gl, ge = _grads(reduction, N, 50)
+    kw = dict(zloss_coef=0.05, softcap=2.5, label_smoothing=0.2, class_weight=cw)
+    out = orc.forward(hidden, weight, labels, reduction, **kw)
+    dh, dw = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, reduction, **kw)
+    eps = 1e-6
+    fd_h = np.zeros_like(hidden)
+    for n in range(N):
+        for h in range(H):
+            hp, hm = hidden.copy(), hidden.copy()
+            hp[n, h] += eps
+            hm[n, h] -= eps
+            fd_h[n, h] = (orc.objective(hp, weight, labels, gl, ge, reduction, **kw)
+                          - orc.objective(hm, weight, labels, gl, ge, reduction, **kw)) / (2 * eps)
+    fd_w = np.zeros_like(weight)
+    for h in range(H):
+        for v in range(V):
+            wp, wm = weight.copy(), weight.copy()
+            wp[h, v] += eps
+            wm[h, v] -= eps
+            fd_w[h, v] = (orc.objective(hidden, wp, labels, gl, ge, reduction, **kw)
+                          - orc.objective(hidden, wm, labels, gl, ge, reduction, **kw)) / (2 * eps)
+    assert np.abs(dh - fd_h).max() / max(1.0, np.abs(fd_h).max()) < 1e-6
+    assert np.abs(dw - fd_w).max() / max(1.0, np.abs(fd_w).max()) < 1e-6
+
+
+@pytest.mark.parametrize("reduction", REDS)
+def test_smoothing_weights_match_scalar_loops(reduction):
+    N, H, V = 5, 4, 7
+    hidden, weight, labels = _rand_case(N, H, V, 60, w_std=0.9, ignore=(1,))
+    cw = np.random.default_rng(60).uniform(0.3, 1.7, V)
+    kw = dict(zloss_coef=0.03, softcap=2.0, label_smoothing=0.15, class_weight=cw)
+    out = orc.forward(hidden, weight, labels, reduction, **kw)
+    l, e, _ = lc.forward_loops(hidden.tolist(), weight.tolist(), labels.tolist(), reduction,
+                               zloss_coef=0.03, softcap=2.0, label_smoothing=0.15,
+                               class_weight=cw.tolist())
+    np.testing.assert_allclose(out["loss"], l, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(out["entropy"], e, rtol=1e-12, atol=1e-13)
+
+
+def test_uniform_class_weights_scale_out_of_the_mean():
+    """Scaling every class weight by a constant leaves the mean loss unchanged
+    (numerator and denominator scale together) and scales the sum."""
+    hidden, weight, labels = _rand_case(20, 6, 30, 70, ignore=(4,))
+    a = orc.forward(hidden, weight, labels, "mean", label_smoothing=0.1)
+    b = orc.forward(hidden, weight, labels, "mean", label_smoothing=0.1,
+                    class_weight=np.full(30, 3.0))
+    np.testing.assert_allclose(b["loss"], a["loss"], rtol=1e-12)
+    c = orc.forward(hidden, weight, labels, "sum", label_smoothing=0.1)
+    d = orc.forward(hidden, weight, labels, "sum", label_smoothing=0.1,
+                    class_weight=np.full(30, 3.0))
+    np.testing.assert_allclose(d["loss"], 3.0 * c["loss"], rtol=1e-12)
