@@ -12,6 +12,12 @@
  *     ent_n   = lse_n - Ez_n                              (entropy of p_n)
  *     loss_n  = ce_n + zloss_coef * lse_n^2               (z-loss: Liger-Kernel PR #435,
  *                                                          "Changes Made"; formula is a reading)
+ *   With label smoothing eps and per-class weights w (options named in the
+ *   Liger-Kernel PR #551 review; defined as torch's cross_entropy(weight,
+ *   label_smoothing)): ce_n = (1-eps) w_{y_n} (lse_n - z_{n,y_n})
+ *                             + eps/V sum_v w_v (lse_n - z_nv);
+ *   the mean then divides the sum of ce_n by the sum of w_{y_n} over non-ignored
+ *   rows, while z-loss and entropy stay unweighted (divided by the row count).
  *   Rows whose label equals ignore_index contribute exactly 0 to loss and entropy
  *   (Liger-Kernel PR #551, review: mean divides by the non-ignored count).
  *   Reduction (Liger-Kernel PR #435, "Summary"): NONE returns loss[N], entropy[N];
@@ -91,6 +97,8 @@ typedef struct {
   int32_t validate;      /* != 0: synchronise at the end and report device errors */
   int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto */
   int32_t weight_layout; /* flce_weight_layout: how weight and dweight are stored */
+  float label_smoothing; /* eps in [0, 1], 0 = off */
+  const float* class_weight; /* [V] fp32 device pointer, per-class target weights; NULL = all 1 */
 } flce_params;
 
 /* Bytes of device workspace that flce_forward (phase 0) or flce_backward (phase 1)

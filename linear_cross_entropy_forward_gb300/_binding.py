@@ -34,7 +34,8 @@ class FlceParams(ctypes.Structure):
                 ("ignore_index", ctypes.c_int64), ("reduction", ctypes.c_int32),
                 ("zloss_coef", ctypes.c_float), ("softcap", ctypes.c_float),
                 ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64),
-                ("weight_layout", ctypes.c_int32)]
+                ("weight_layout", ctypes.c_int32), ("label_smoothing", ctypes.c_float),
+                ("class_weight", ctypes.c_void_p)]
 
 
 WEIGHT_HV, WEIGHT_VH = 0, 1
@@ -93,10 +94,13 @@ def _check(code: int):
 
 
 def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
-                softcap=0.0, validate=False, chunk_v=0, weight_layout="hv") -> FlceParams:
+                softcap=0.0, validate=False, chunk_v=0, weight_layout="hv",
+                label_smoothing=0.0, class_weight=None) -> FlceParams:
+    """class_weight: a CUDA fp32 [V] tensor (kept alive by the caller) or None."""
+    cw = class_weight.data_ptr() if class_weight is not None else None
     return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
                       float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v),
-                      layout_code(weight_layout))
+                      layout_code(weight_layout), float(label_smoothing), cw)
 
 
 def _dims(hidden, weight, weight_layout):
@@ -147,20 +151,24 @@ def _workspace(params, phase, device, workspace):
 
 def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
                  zloss_coef=0.0, softcap=0.0, validate=False, workspace=None, stream=None,
-                 out=None, weight_layout="hv"):
+                 out=None, weight_layout="hv", label_smoothing=0.0, class_weight=None):
     """Forward pass through the C ABI.
 
     Returns (loss, entropy, lse, ez): loss/entropy are [N] for reduction 'none'
     and [1] otherwise; lse/ez are the per-row [N] statistics saved for backward.
-    weight is [H,V] (weight_layout 'hv') or [V,H] ('vh', nn.Linear).
+    weight is [H,V] (weight_layout 'hv') or [V,H] ('vh', nn.Linear).  label_smoothing
+    and class_weight (CUDA fp32 [V]) follow torch's cross_entropy definitions.
     """
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
     _need(weight, "weight", torch.bfloat16, wshape)
     _need(labels, "labels", torch.int64, (N,))
+    if class_weight is not None:
+        _need(class_weight, "class_weight", torch.float32, (V,))
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
-                    weight_layout=weight_layout)
+                    weight_layout=weight_layout, label_smoothing=label_smoothing,
+                    class_weight=class_weight)
     dev = hidden.device
     n_out = N if p.reduction == RED_NONE else 1
     if out is None:
@@ -179,7 +187,8 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
 
 def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
                   ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, validate=False,
-                  chunk_v=0, workspace=None, stream=None, out=None, weight_layout="hv"):
+                  chunk_v=0, workspace=None, stream=None, out=None, weight_layout="hv",
+                  label_smoothing=0.0, class_weight=None):
     """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight bf16 shaped
     like weight).
 
@@ -192,8 +201,10 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     _need(labels, "labels", torch.int64, (N,))
     _need(lse, "lse", torch.float32, (N,))
     _need(ez, "ez", torch.float32, (N,))
+    if class_weight is not None:
+        _need(class_weight, "class_weight", torch.float32, (V,))
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v,
-                    weight_layout)
+                    weight_layout, label_smoothing, class_weight)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
         _need(g_loss, "g_loss", torch.float32, (n_g,))
@@ -220,11 +231,14 @@ def flce_status(workspace, stream=None) -> int:
 class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap,
-                weight_layout):
+                weight_layout, label_smoothing, class_weight):
         loss, ent, lse, ez = flce_forward(hidden, weight, labels, reduction, ignore_index,
-                                          zloss_coef, softcap, weight_layout=weight_layout)
+                                          zloss_coef, softcap, weight_layout=weight_layout,
+                                          label_smoothing=label_smoothing,
+                                          class_weight=class_weight)
         ctx.save_for_backward(hidden, weight, labels, lse, ez)
-        ctx.cfg = (reduction, ignore_index, zloss_coef, softcap, weight_layout)
+        ctx.cfg = (reduction, ignore_index, zloss_coef, softcap, weight_layout,
+                   label_smoothing, class_weight)
         if reduction_code(reduction) != RED_NONE:
             loss, ent = loss[0], ent[0]
         return loss, ent
@@ -232,7 +246,8 @@ class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g_loss, g_ent):
         hidden, weight, labels, lse, ez = ctx.saved_tensors
-        reduction, ignore_index, zloss_coef, softcap, weight_layout = ctx.cfg
+        (reduction, ignore_index, zloss_coef, softcap, weight_layout, label_smoothing,
+         class_weight) = ctx.cfg
         n_g = hidden.shape[0] if reduction_code(reduction) == RED_NONE else 1
 
         def prep(g):
@@ -242,18 +257,23 @@ class _LinearCrossEntropy(torch.autograd.Function):
 
         dh, dw = flce_backward(hidden, weight, labels, lse, ez, prep(g_loss), prep(g_ent),
                                reduction, ignore_index, zloss_coef, softcap,
-                               weight_layout=weight_layout)
-        return dh, dw, None, None, None, None, None, None
+                               weight_layout=weight_layout, label_smoothing=label_smoothing,
+                               class_weight=class_weight)
+        return dh, dw, None, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
-                         zloss_coef=0.0, softcap=0.0, weight_layout="hv"):
+                         zloss_coef=0.0, softcap=0.0, weight_layout="hv", label_smoothing=0.0,
+                         class_weight=None):
     """loss, entropy = linear_cross_entropy(hidden, weight, labels, reduction)
 
     The call of verl PR #462 ("API"): hidden [N,H] bf16, weight [H,V] bf16,
     labels [N] int64.  `loss` is the cross-entropy (+ z-loss); the page's
     log-probability is -loss when z-loss is off.  Differentiable w.r.t. hidden
-    and weight.  weight_layout='vh' takes an nn.Linear-style weight [V,H].
+    and weight.  weight_layout='vh' takes an nn.Linear-style weight [V,H];
+    label_smoothing and class_weight (fp32 [V], not differentiated) follow torch's
+    cross_entropy.
     """
     return _LinearCrossEntropy.apply(hidden, weight, labels, reduction, ignore_index,
-                                     zloss_coef, softcap, weight_layout)
+                                     zloss_coef, softcap, weight_layout, label_smoothing,
+                                     class_weight)

@@ -48,32 +48,48 @@ __device__ __forceinline__ void merge_stats(float& M, float& D, float& S, float 
 }
 
 // One block of 8 warps handles 32 rows; warp w merges parts w, w+8, ...
+// Label smoothing / class weights of the combine (Smoothing.eps == 0 and cw == NULL:
+// plain cross-entropy).  psw holds the partial sums_v w_v z_v, wsum = sum_v w_v.
+struct Smoothing {
+  float eps;
+  const float* cw;
+  const float* psw;
+  const float* wsum;  // device scalar (NULL: V, all weights 1)
+};
+
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     const float* __restrict__ pm, const float* __restrict__ pd, const float* __restrict__ ps,
     int64_t n_parts, int64_t N, const float* __restrict__ zlabel,
     const int64_t* __restrict__ labels, int64_t V, int64_t ignore_index, float zcoef,
-    float* __restrict__ lse_out, float* __restrict__ ez_out, float* __restrict__ loss_row,
-    float* __restrict__ ent_row, uint32_t* err) {
-  __shared__ float sM[8][32], sD[8][32], sS[8][32];
+    Smoothing sm, float* __restrict__ lse_out, float* __restrict__ ez_out,
+    float* __restrict__ loss_row, float* __restrict__ ent_row, uint32_t* err) {
+  __shared__ float sM[8][32], sD[8][32], sS[8][32], sW[8][32];
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  float M = -1e30f, D = 0.0f, S = 0.0f;
+  const bool smooth = sm.eps != 0.0f;
+  float M = -1e30f, D = 0.0f, S = 0.0f, SW = 0.0f;
   if (n < N) {
     for (int64_t p = w; p < n_parts; p += 8) {
       const int64_t o = p * N + n;
       merge_stats(M, D, S, pm[o], pd[o], ps[o]);
+      if (smooth) SW += sm.psw[o];
     }
   }
   sM[w][lane] = M;
   sD[w][lane] = D;
   sS[w][lane] = S;
+  sW[w][lane] = SW;
   __syncthreads();
   if (w != 0 || n >= N) return;
   M = sM[0][lane];
   D = sD[0][lane];
   S = sS[0][lane];
-  for (int k = 1; k < 8; ++k) merge_stats(M, D, S, sM[k][lane], sD[k][lane], sS[k][lane]);
+  SW = sW[0][lane];
+  for (int k = 1; k < 8; ++k) {
+    merge_stats(M, D, S, sM[k][lane], sD[k][lane], sS[k][lane]);
+    SW += sW[k][lane];
+  }
   // M, S in log2 units: lse = ln2 (M + log2 D); entropy = ln d - s_c/d = ln2 (log2 D - S/D)
   const float l2d = log2f(D);
   const float lse = kLn2 * (M + l2d);
@@ -87,7 +103,15 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
       atomicOr(err, FLCE_DEVERR_LABEL);
       lt = et = __int_as_float(0x7fc00000);
     } else {
-      lt = (lse - zlabel[n]) + zcoef * lse * lse;
+      float ce = lse - zlabel[n];
+      if (smooth || sm.cw) {
+        // (1 - eps) w_y (lse - z_y) + eps/V (W lse - sum_v w_v z_v)
+        const float wy = sm.cw ? sm.cw[y] : 1.0f;
+        const float W = sm.wsum ? *sm.wsum : static_cast<float>(V);
+        ce = (1.0f - sm.eps) * wy * ce;
+        if (smooth) ce += sm.eps / static_cast<float>(V) * (W * lse - SW);
+      }
+      lt = ce + zcoef * lse * lse;
       et = ent;
     }
   }
@@ -96,27 +120,42 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
 }
 
 // Deterministic fixed-order reduction over rows (one block): mean or sum.
+// With class weights cw the mean divides the cross-entropy part of the rows
+// (loss_row - zcoef lse^2) by the summed w_y and the z-loss part by the row count.
 __global__ void __launch_bounds__(1024) reduce_rows_kernel(
     const float* __restrict__ loss_row, const float* __restrict__ ent_row,
     const int64_t* __restrict__ labels, int64_t N, int64_t ignore_index, int mean,
+    const float* __restrict__ cw, const float* __restrict__ lse, float zcoef,
     float* __restrict__ loss_out, float* __restrict__ ent_out) {
-  __shared__ double sl[1024], se[1024];
+  __shared__ double sl[1024], se[1024], sz[1024], sw[1024];
   __shared__ long long sc[1024];
-  double l = 0.0, e = 0.0;
+  double l = 0.0, e = 0.0, zl = 0.0, wsum = 0.0;
   long long c = 0;
   for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
     l += loss_row[n];
     e += ent_row[n];
-    c += labels[n] != ignore_index;
+    const int64_t y = labels[n];
+    if (y != ignore_index) {
+      ++c;
+      if (cw) {
+        const double ln = lse[n];
+        zl += static_cast<double>(zcoef) * ln * ln;
+        wsum += cw[y];
+      }
+    }
   }
   sl[threadIdx.x] = l;
   se[threadIdx.x] = e;
+  sz[threadIdx.x] = zl;
+  sw[threadIdx.x] = wsum;
   sc[threadIdx.x] = c;
   __syncthreads();
   for (int s = blockDim.x / 2; s > 0; s >>= 1) {
     if (threadIdx.x < s) {
       sl[threadIdx.x] += sl[threadIdx.x + s];
       se[threadIdx.x] += se[threadIdx.x + s];
+      sz[threadIdx.x] += sz[threadIdx.x + s];
+      sw[threadIdx.x] += sw[threadIdx.x + s];
       sc[threadIdx.x] += sc[threadIdx.x + s];
     }
     __syncthreads();
@@ -125,41 +164,99 @@ __global__ void __launch_bounds__(1024) reduce_rows_kernel(
     double L = sl[0], E = se[0];
     if (mean) {
       const long long nv = sc[0];
-      L = nv > 0 ? L / static_cast<double>(nv) : 0.0;
-      E = nv > 0 ? E / static_cast<double>(nv) : 0.0;
+      const double rn = nv > 0 ? 1.0 / static_cast<double>(nv) : 0.0;
+      if (cw) {
+        const double ce = L - sz[0];
+        L = (sw[0] != 0.0 ? ce / sw[0] : 0.0) + sz[0] * rn;
+      } else {
+        L = L * rn;
+      }
+      E = E * rn;
     }
     loss_out[0] = static_cast<float>(L);
     ent_out[0] = static_cast<float>(E);
   }
 }
 
-// Per-row constants of the dlogits epilogue:
-// (lse*log2e, a (1 + 2 coef lse) + b Ez, b, a), a/b the scaled upstream grads.
+// wsum[0] = sum_v cw[v] (one block, fixed order).
+__global__ void __launch_bounds__(1024) class_weight_sum_kernel(const float* __restrict__ cw,
+                                                                int64_t V, float* wsum) {
+  __shared__ double sw[1024];
+  double a = 0.0;
+  for (int64_t v = threadIdx.x; v < V; v += blockDim.x) a += cw[v];
+  sw[threadIdx.x] = a;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) sw[threadIdx.x] += sw[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) wsum[0] = static_cast<float>(sw[0]);
+}
+
+// Per-row constants of the dlogits epilogue, with a_ce / a_z / b the upstream
+// gradients of the cross-entropy part, the z-loss and the entropy after the
+// reduction (mean: a_ce / sum w_y, a_z and b / n_valid) and zero on ignored rows:
+//   rowc = (lse log2e, A1, b, C_y),  rowd = D,  where
+//   A1 = a_ce ((1 - eps) w_y + eps W / V) + 2 coef lse a_z + b Ez,
+//   C_y = a_ce (1 - eps) w_y,  D = a_ce eps / V,
+// so that dlogits = p (A1 - b z) - C_y [v == y] - D w_v.
 __global__ void __launch_bounds__(1024) bwd_prep_kernel(
     const int64_t* __restrict__ labels, const float* __restrict__ lse,
     const float* __restrict__ ez, const float* __restrict__ g_loss,
-    const float* __restrict__ g_ent, int64_t N, int64_t ignore_index, int per_token, int mean,
-    float zcoef, float4* __restrict__ rowc) {
+    const float* __restrict__ g_ent, int64_t N, int64_t V, int64_t ignore_index, int per_token,
+    int mean, float zcoef, float eps, const float* __restrict__ cw, float4* __restrict__ rowc,
+    float* __restrict__ rowd) {
   __shared__ long long sc[1024];
+  __shared__ double sw[1024], sww[1024];
   long long c = 0;
-  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) c += labels[n] != ignore_index;
+  double wy_sum = 0.0, w_all = 0.0;
+  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+    const int64_t y = labels[n];
+    if (y != ignore_index) {
+      ++c;
+      if (cw) wy_sum += cw[y];
+    }
+  }
+  if (cw && eps != 0.0f)
+    for (int64_t v = threadIdx.x; v < V; v += blockDim.x) w_all += cw[v];
   sc[threadIdx.x] = c;
+  sw[threadIdx.x] = wy_sum;
+  sww[threadIdx.x] = w_all;
   __syncthreads();
   for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if (threadIdx.x < s) sc[threadIdx.x] += sc[threadIdx.x + s];
+    if (threadIdx.x < s) {
+      sc[threadIdx.x] += sc[threadIdx.x + s];
+      sw[threadIdx.x] += sw[threadIdx.x + s];
+      sww[threadIdx.x] += sww[threadIdx.x + s];
+    }
     __syncthreads();
   }
   const long long nv = sc[0];
   const float scale = mean ? (nv > 0 ? 1.0f / static_cast<float>(nv) : 0.0f) : 1.0f;
+  const bool plain = eps == 0.0f && cw == nullptr;
+  const float scale_ce =
+      (mean && cw) ? (sw[0] != 0.0 ? static_cast<float>(1.0 / sw[0]) : 0.0f) : scale;
+  const float W = cw ? static_cast<float>(sww[0]) : static_cast<float>(V);
   for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
-    const bool valid = labels[n] != ignore_index;
+    const int64_t y = labels[n];
+    const bool valid = y != ignore_index;
     const int64_t gi = per_token ? n : 0;
     const float gl = g_loss ? g_loss[gi] : 0.0f;
     const float ge = g_ent ? g_ent[gi] : 0.0f;
     const float a = valid ? gl * scale : 0.0f;
     const float b = valid ? ge * scale : 0.0f;
     const float l = lse[n];
-    rowc[n] = make_float4(l * kLog2e, fmaf(a, fmaf(2.0f * zcoef, l, 1.0f), b * ez[n]), b, a);
+    if (plain) {
+      rowc[n] = make_float4(l * kLog2e, fmaf(a, fmaf(2.0f * zcoef, l, 1.0f), b * ez[n]), b, a);
+      continue;
+    }
+    const float a_ce = valid ? gl * scale_ce : 0.0f;
+    const float wy = (cw && valid && y >= 0 && y < V) ? cw[y] : 1.0f;
+    const float cy = a_ce * (1.0f - eps) * wy;
+    const float a1 = fmaf(a_ce, eps * W / static_cast<float>(V), cy) +
+                     fmaf(2.0f * zcoef * l, a, b * ez[n]);
+    rowc[n] = make_float4(l * kLog2e, a1, b, cy);
+    if (eps != 0.0f) rowd[n] = a_ce * eps / static_cast<float>(V);
   }
 }
 
@@ -168,9 +265,11 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct FwdLayout {
-  size_t pm, pd, ps, zlabel, loss_row, ent_row, total;
+  size_t pm, pd, ps, psw, zlabel, loss_row, ent_row, total;
   int64_t n_parts;
 };
+
+constexpr size_t kWsumOffset = 64;  // float in the workspace header: sum of class weights
 
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
@@ -181,6 +280,8 @@ FwdLayout fwd_layout(const flce_params* p) {
   L.pm = off; off += part_bytes;
   L.pd = off; off += part_bytes;
   L.ps = off; off += part_bytes;
+  L.psw = off;
+  if (p->label_smoothing != 0.0f) off += part_bytes;
   L.zlabel = off; off += row_bytes;
   L.loss_row = off; off += row_bytes;
   L.ent_row = off; off += row_bytes;
@@ -189,7 +290,7 @@ FwdLayout fwd_layout(const flce_params* p) {
 }
 
 struct BwdLayout {
-  size_t rowc, dl, acc, total;
+  size_t rowc, rowd, dl, acc, total;
   int64_t Vc, chunks;
 };
 
@@ -212,6 +313,8 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.chunks = cdiv(p->V, L.Vc);
   size_t off = kHeaderBytes;
   L.rowc = off; off += align256(static_cast<size_t>(p->N) * 16);
+  L.rowd = off;
+  if (p->label_smoothing != 0.0f) off += align256(static_cast<size_t>(p->N) * 4);
   L.dl = off; off += align256(static_cast<size_t>(p->N) * L.Vc * 2);
   L.acc = off;
   if (L.chunks > 1) off += align256(static_cast<size_t>(p->N) * p->H * 4);
@@ -229,6 +332,8 @@ int check_params(const flce_params* p) {
   if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % 256 != 0)) return FLCE_ERR_BAD_ARG;
   if (p->weight_layout != FLCE_WEIGHT_HV && p->weight_layout != FLCE_WEIGHT_VH)
     return FLCE_ERR_BAD_ARG;
+  if (!(p->label_smoothing >= 0.0f && p->label_smoothing <= 1.0f)) return FLCE_ERR_BAD_ARG;
+  if (reinterpret_cast<uintptr_t>(p->class_weight) & 3) return FLCE_ERR_ALIGN;
   // chunk-relative and vocabulary column indices are 32-bit inside the kernels
   if (cdiv(p->V, 256) * 256 > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   return FLCE_OK;
@@ -439,19 +544,30 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   ea.ps = reinterpret_cast<float*>(ws + L.ps);
   ea.part_stride = N;
   ea.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
+  ea.smooth = p->label_smoothing;
+  ea.cw = p->class_weight;
+  ea.psw = reinterpret_cast<float*>(ws + L.psw);
   ea.err = err;
   if ((rc = cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st))))
     return rc;
+  Smoothing sm{p->label_smoothing, p->class_weight, ea.psw, nullptr};
+  if (p->label_smoothing != 0.0f && p->class_weight) {
+    float* wsum = reinterpret_cast<float*>(ws + kWsumOffset);
+    class_weight_sum_kernel<<<1, 1024, 0, st>>>(p->class_weight, V, wsum);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+    sm.wsum = wsum;
+  }
 
   float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
   float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
   fwd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 32)), 256, 0, st>>>(
       ea.pm, ea.pd, ea.ps, L.n_parts, N, ea.zlabel, labels, V, p->ignore_index, p->zloss_coef,
-      lse, ez, loss_row, ent_row, err);
+      sm, lse, ez, loss_row, ent_row, err);
   if ((rc = cuda_rc(cudaGetLastError()))) return rc;
   if (!per_token) {
     reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,
-                                           p->reduction == FLCE_RED_MEAN, loss, entropy);
+                                           p->reduction == FLCE_RED_MEAN, p->class_weight,
+                                           lse, p->zloss_coef, loss, entropy);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
   }
   return p->validate ? read_status(ws, st) : FLCE_OK;
@@ -490,9 +606,11 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   float4* rowc = reinterpret_cast<float4*>(ws + L.rowc);
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + L.dl);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
-  bwd_prep_kernel<<<1, 1024, 0, st>>>(labels, lse, ez, g_loss, g_entropy, N, p->ignore_index,
+  float* rowd = reinterpret_cast<float*>(ws + L.rowd);
+  bwd_prep_kernel<<<1, 1024, 0, st>>>(labels, lse, ez, g_loss, g_entropy, N, V, p->ignore_index,
                                       p->reduction == FLCE_RED_NONE,
-                                      p->reduction == FLCE_RED_MEAN, p->zloss_coef, rowc);
+                                      p->reduction == FLCE_RED_MEAN, p->zloss_coef,
+                                      p->label_smoothing, p->class_weight, rowc, rowd);
   if ((rc = cuda_rc(cudaGetLastError()))) return rc;
 
   // Operand tensor maps.  hidden: K-major (recompute) and MN-major (dweight);
@@ -533,6 +651,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e3.labels = labels;
     e3.ignore_index = p->ignore_index;
     e3.rowc = rowc;
+    e3.rowd = rowd;
+    e3.smooth = p->label_smoothing;
+    e3.cw = p->class_weight;
     e3.dl = dl;
     e3.ld_dl = L.Vc;
     e3.err = err;

@@ -105,8 +105,14 @@ struct EpiArgs {
   float* ps;
   int64_t part_stride;  // elements between consecutive column parts
   float* zlabel;
+  // label smoothing (FWD_STATS and DLOGITS): eps != 0 turns it on; cw are the
+  // per-class weights (NULL: all 1)
+  float smooth;
+  const float* cw;
+  float* psw;           // FWD_STATS: per part sum_v w_v z_v (same layout as pm)
   // EPI_DLOGITS
-  const float4* rowc;   // per row: (lse*log2e, a(1+2 coef lse) + b Ez, b, a)
+  const float4* rowc;   // per row: (lse*log2e, A1, b, C_y), see bwd_prep_kernel
+  const float* rowd;    // per row: D, the coefficient of -w_v (label smoothing)
   __nv_bfloat16* dl;
   int64_t ld_dl;
   // EPI_STORE_BF16
@@ -173,7 +179,8 @@ struct Epilogue<EPI_FWD_STATS> {
     const bool cap = ea.softcap != 0.0f;
     const float inv_cap = cap ? 1.0f / ea.softcap : 0.0f;
     const int vcol0 = ea.col_base + col0;
-    float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f;
+    const bool smooth = ea.smooth != 0.0f;
+    float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f, sw = 0.0f;
     bool hit = false;
 #pragma unroll 1
     for (int c = 0; c < CH; ++c) {
@@ -181,11 +188,19 @@ struct Epilogue<EPI_FWD_STATS> {
       tmem_ld32(tbase + c * 32, x);
       const int vb = vcol0 + c * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
+      if (cap) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = ea.softcap * tanh_from_exp(x[j] * inv_cap);
+      }
+      if (smooth) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
+      }
       float cm = -1e30f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float z = x[j];
-        if (cap) z = ea.softcap * tanh_from_exp(z * inv_cap);
+        const float z = x[j];
         if (vb + j == y) {
           zy = z;
           hit = true;
@@ -224,6 +239,7 @@ struct Epilogue<EPI_FWD_STATS> {
       ea.pm[o] = mx;
       ea.pd[o] = d;
       ea.ps[o] = s;
+      if (smooth) ea.psw[o] = sw;
       if (hit) ea.zlabel[row] = zy;
     }
   }
@@ -236,10 +252,13 @@ struct Epilogue<EPI_DLOGITS> {
   static __device__ __forceinline__ void run(const EpiArgs& ea, uint32_t tbase, int row,
                                              int col0) {
     const bool row_ok = row < ea.rows;
+    const bool smooth = ea.smooth != 0.0f;
     float4 rc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float dcoef = 0.0f;
     int y = -1;
     if (row_ok) {
       rc = ea.rowc[row];
+      if (smooth) dcoef = ea.rowd[row];
       int64_t yl = ea.labels[row];
       if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
     }
@@ -268,6 +287,8 @@ struct Epilogue<EPI_DLOGITS> {
           const float p = fast_ex2(fmaf(z, kLog2e, -rc.x));
           float g = p * fmaf(-rc.z, z, rc.y);
           if (vb + j + h == y) g -= rc.w;
+          if (smooth && j + h < nvalid)
+            g = fmaf(-dcoef, ea.cw ? __ldg(ea.cw + vb + j + h) : 1.0f, g);
           if (cap) g *= fmaf(-th, th, 1.0f);
           g2[h] = (j + h < nvalid) ? g : 0.0f;
         }

@@ -42,10 +42,12 @@ def test_version_and_strerror(lib):
 
 
 def test_params_struct_layout():
-    # int64 x4, int32, float, float, int32, int64, int32 (+4 padding) -> 64 bytes, as in flce.h
-    assert ctypes.sizeof(B.FlceParams) == 64
+    # int64 x4, int32, float, float, int32, int64, int32, float, pointer -> 72 bytes (flce.h)
+    assert ctypes.sizeof(B.FlceParams) == 72
     assert B.FlceParams.chunk_v.offset == 48
     assert B.FlceParams.weight_layout.offset == 56
+    assert B.FlceParams.label_smoothing.offset == 60
+    assert B.FlceParams.class_weight.offset == 64
 
 
 def test_workspace_sizes(lib):
@@ -72,6 +74,8 @@ def test_workspace_sizes(lib):
     (dict(N=10, H=64, V=64, chunk_v=100), 1),
     (dict(N=10, H=64, V=64, zloss_coef=-1.0), 1),
     (dict(N=10, H=64, V=64, weight_layout=7), 1),
+    (dict(N=10, H=64, V=64, label_smoothing=1.5), 1),
+    (dict(N=10, H=64, V=64, label_smoothing=-0.1), 1),
 ])
 def test_bad_params_rejected_on_host(lib, kw, code):
     args = dict(N=10, H=64, V=64)

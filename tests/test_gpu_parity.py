@@ -37,23 +37,27 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
 
 
-def oracle_run(w, hidden, weight, labels, g_loss, g_ent):
+def oracle_run(w, hidden, weight, labels, g_loss, g_ent, eps=0.0, cw=None):
     h = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
     W = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
     y = labels.numpy()
-    o = orc.forward(h, W, y, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, label_smoothing=eps,
+              class_weight=None if cw is None else cw.numpy())
+    o = orc.forward(h, W, y, w.reduction, **kw)
     dh, dw = orc.backward(h, W, y, o["lse"], o["ez"], g_loss.numpy(), g_ent.numpy(), w.reduction,
-                          zloss_coef=w.zloss_coef, softcap=w.softcap)
+                          **kw)
     return o, dh, dw
 
 
-def gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v=0, weight_layout="hv"):
+def gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v=0, weight_layout="hv", eps=0.0,
+            cw=None):
     """weight is [H,V]; with weight_layout 'vh' the GPU gets its [V,H] transpose and the
     returned dw is transposed back to [H,V]."""
     dev = torch.device("cuda")
     hd, yd = hidden.to(dev), labels.to(dev)
     Wd = weight.to(dev) if weight_layout == "hv" else weight.t().contiguous().to(dev)
-    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=weight_layout)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=weight_layout,
+              label_smoothing=eps, class_weight=None if cw is None else cw.to(dev))
     loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True, **kw)
     dh, dw = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
                            validate=True, chunk_v=chunk_v, **kw)
@@ -66,10 +70,10 @@ def gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v=0, weight_layout="
                 dh_raw=dh.cpu())
 
 
-def check_parity(w, chunk_v=0, report=None, weight_layout="hv"):
+def check_parity(w, chunk_v=0, report=None, weight_layout="hv", eps=0.0, cw=None):
     hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
-    o, dh_o, dw_o = oracle_run(w, hidden, weight, labels, g_loss, g_ent)
-    g = gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v, weight_layout)
+    o, dh_o, dw_o = oracle_run(w, hidden, weight, labels, g_loss, g_ent, eps, cw)
+    g = gpu_run(w, hidden, weight, labels, g_loss, g_ent, chunk_v, weight_layout, eps, cw)
     valid = o["valid"]
     errs = {}
     errs["lse_abs"] = float(np.abs(g["lse"] - o["lse"]).max())
@@ -149,6 +153,34 @@ def test_parity_weight_vh(name, w, chunk_v):
     rep = {}
     check_parity(w, chunk_v, rep, weight_layout="vh")
     print(name, "vh", rep)
+
+
+SMOOTH_CASES = [
+    # (name, workload, chunk_v, label_smoothing, class weights?)
+    ("smooth_mean", dataclasses.replace(W0, name="ls1", N=300, H=200, V=1000), 256, 0.1, False),
+    ("weights_mean", dataclasses.replace(W0, name="ls2", N=300, H=200, V=1000), 512, 0.0, True),
+    ("smooth_weights_none", dataclasses.replace(W0, name="ls3", N=260, H=128, V=776,
+                                                reduction="none", grad_mode="normal"),
+     256, 0.2, True),
+    ("smooth_weights_sum_zloss_cap", dataclasses.replace(W0, name="ls4", N=384, H=256, V=2048,
+                                                         reduction="sum", zloss_coef=1e-2,
+                                                         softcap=3.0, w_std=0.2), 512, 0.05, True),
+    ("smooth_weights_mean_zloss", dataclasses.replace(W0, name="ls5", N=256, H=512, V=4096,
+                                                      zloss_coef=1e-4), 0, 0.1, True),
+]
+
+
+@pytest.mark.parametrize("name,w,chunk_v,eps,weighted", SMOOTH_CASES,
+                         ids=[c[0] for c in SMOOTH_CASES])
+def test_parity_smoothing_and_class_weights(name, w, chunk_v, eps, weighted):
+    _cuda_or_skip()
+    cw = None
+    if weighted:
+        g = torch.Generator().manual_seed(123)
+        cw = torch.rand(w.V, generator=g) * 1.5 + 0.25
+    rep = {}
+    check_parity(w, chunk_v, rep, eps=eps, cw=cw)
+    print(name, rep)
 
 
 def test_layouts_agree_bitwise():
