@@ -99,11 +99,18 @@ typedef struct {
   int32_t weight_layout; /* flce_weight_layout: how weight and dweight are stored */
   float label_smoothing; /* eps in [0, 1], 0 = off */
   const float* class_weight; /* [V] fp32 device pointer, per-class target weights; NULL = all 1 */
+  /* Vocabulary sharding (see flce_shard_stats).  v_total = 0: weight holds the whole
+   * vocabulary.  v_total > 0: weight holds columns [v_offset, v_offset + V) of a
+   * vocabulary of v_total entries, and labels are indices into the whole vocabulary.
+   * Sharding excludes label_smoothing and class_weight. */
+  int64_t v_offset;
+  int64_t v_total;
 } flce_params;
 
-/* Bytes of device workspace that flce_forward (phase 0) or flce_backward (phase 1)
- * needs for these parameters; 0 when the parameters are invalid.  The workspace is
- * scratch: its contents need not be preserved between calls. */
+/* Bytes of device workspace that flce_forward / flce_shard_stats (phase 0),
+ * flce_backward (phase 1) or flce_combine_shards (phase 2) needs for these
+ * parameters; 0 when the parameters are invalid.  The workspace is scratch: its
+ * contents need not be preserved between calls. */
 size_t flce_workspace_size(const flce_params* params, int phase);
 
 /* Forward pass.
@@ -128,13 +135,37 @@ int flce_backward(const flce_params* params, const void* hidden, const void* wei
                   const float* g_loss, const float* g_entropy, void* dhidden, void* dweight,
                   void* workspace, size_t ws_bytes, void* stream);
 
+/* Vocabulary-parallel forward, step 1 (the softmax statistics are split over
+ * shards of the vocabulary and merged with the online-softmax max-rescale).
+ *   params: V, v_offset, v_total describe this shard; weight is its slice, stored
+ *   as params->weight_layout says ([H,V] or [V,H] with V the shard width).
+ *   stats: [4, N] fp32, overwritten: per row, over the shard's columns, the maximum
+ *   m of log2e * z, d = sum 2^(log2e z - m), s = sum 2^(log2e z - m) (log2e z - m),
+ *   and the label's logit z_y if the label falls in the shard (else 0).
+ *   workspace: >= flce_workspace_size(params, 0) bytes. */
+int flce_shard_stats(const flce_params* params, const void* hidden, const void* weight,
+                     const int64_t* labels, float* stats, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/* Vocabulary-parallel forward, step 2: merge the stats of all shards.
+ *   stats: [n_shards, 4, N] fp32, each shard's flce_shard_stats output (as an
+ *   all-gather across ranks produces it).  Outputs as flce_forward's, for the whole
+ *   vocabulary (params->v_total entries).  workspace: >= flce_workspace_size(params, 2).
+ * The backward of a shard is flce_backward with the same sharded params and weight
+ * slice: it writes that shard's dweight and this shard's term of dhidden, which the
+ * caller sums over the shards. */
+int flce_combine_shards(const flce_params* params, const float* stats, int32_t n_shards,
+                        const int64_t* labels, float* loss, float* entropy, float* lse,
+                        float* ez, void* workspace, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device-side status recorded in the
  * workspace header by the last call that used this workspace (FLCE_OK,
  * FLCE_ERR_LABEL or FLCE_ERR_TIMEOUT), or FLCE_ERR_CUDA. */
 int flce_status(const void* workspace, void* stream);
 
-/* Number of kernels one flce_forward (phase 0) or flce_backward (phase 1) call
- * with these parameters enqueues (memsets not counted); -1 when invalid. */
+/* Number of kernels one call with these parameters enqueues (memsets not counted):
+ * phase 0 flce_forward, 1 flce_backward, 2 flce_combine_shards, 3 flce_shard_stats;
+ * -1 when invalid. */
 int flce_kernel_launches(const flce_params* params, int phase);
 
 /* Static, NUL-terminated description of a status code. */

@@ -6,10 +6,12 @@ The [N, V] logits are never materialised: tcgen05 tensor-core GEMM tiles feed
 fused online-softmax (forward) and dlogits (backward) epilogues inside
 libflce.so, reached through a C ABI (include/flce.h).
 """
-from ._binding import (FlceError, FlceParams, flce_backward, flce_forward,  # noqa: F401
-                       flce_status, kernel_launches, linear_cross_entropy, load_library,
-                       make_params,
-                       workspace_size, LIB_PATH, EXPORTED)
+from ._binding import (FlceError, FlceParams, flce_backward, flce_combine_shards,  # noqa: F401
+                       flce_forward, flce_shard_stats, flce_status, kernel_launches,
+                       linear_cross_entropy, load_library, make_params, workspace_size,
+                       LIB_PATH, EXPORTED)
+from .vocab_parallel import (exchange_stats, reduce_dhidden,  # noqa: F401
+                             vocab_parallel_linear_cross_entropy)
 from .workloads import IGNORE_INDEX, WORKLOADS  # noqa: F401
 
 __version__ = "0.1.0"

@@ -35,7 +35,8 @@ class FlceParams(ctypes.Structure):
                 ("zloss_coef", ctypes.c_float), ("softcap", ctypes.c_float),
                 ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64),
                 ("weight_layout", ctypes.c_int32), ("label_smoothing", ctypes.c_float),
-                ("class_weight", ctypes.c_void_p)]
+                ("class_weight", ctypes.c_void_p), ("v_offset", ctypes.c_int64),
+                ("v_total", ctypes.c_int64)]
 
 
 WEIGHT_HV, WEIGHT_VH = 0, 1
@@ -54,7 +55,8 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
-            "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc")
+            "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc",
+            "flce_shard_stats", "flce_combine_shards")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -80,6 +82,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flce_status.restype = ctypes.c_int
         lib.flce_strerror.argtypes = [ctypes.c_int]
         lib.flce_strerror.restype = ctypes.c_char_p
+        lib.flce_shard_stats.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.flce_shard_stats.restype = ctypes.c_int
+        lib.flce_combine_shards.argtypes = [P, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp,
+                                            ctypes.c_size_t, vp]
+        lib.flce_combine_shards.restype = ctypes.c_int
         lib.flce_kernel_launches.argtypes = [P, ctypes.c_int]
         lib.flce_kernel_launches.restype = ctypes.c_int
         lib.flce_version.argtypes = []
@@ -95,12 +102,15 @@ def _check(code: int):
 
 def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
                 softcap=0.0, validate=False, chunk_v=0, weight_layout="hv",
-                label_smoothing=0.0, class_weight=None) -> FlceParams:
-    """class_weight: a CUDA fp32 [V] tensor (kept alive by the caller) or None."""
+                label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0) -> FlceParams:
+    """class_weight: a CUDA fp32 [V] tensor (kept alive by the caller) or None.
+    v_offset / v_total: this weight is columns [v_offset, v_offset + V) of a vocabulary
+    of v_total entries (0: the whole vocabulary)."""
     cw = class_weight.data_ptr() if class_weight is not None else None
     return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
                       float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v),
-                      layout_code(weight_layout), float(label_smoothing), cw)
+                      layout_code(weight_layout), float(label_smoothing), cw, int(v_offset),
+                      int(v_total))
 
 
 def _dims(hidden, weight, weight_layout):
@@ -188,11 +198,13 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
 def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
                   ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, validate=False,
                   chunk_v=0, workspace=None, stream=None, out=None, weight_layout="hv",
-                  label_smoothing=0.0, class_weight=None):
+                  label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0):
     """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight bf16 shaped
     like weight).
 
     g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
+    With a vocabulary shard (v_total > 0) dweight is the shard's and dhidden is the
+    shard's term of the sum over shards.
     """
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
@@ -204,7 +216,7 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     if class_weight is not None:
         _need(class_weight, "class_weight", torch.float32, (V,))
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v,
-                    weight_layout, label_smoothing, class_weight)
+                    weight_layout, label_smoothing, class_weight, v_offset, v_total)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
         _need(g_loss, "g_loss", torch.float32, (n_g,))
@@ -221,6 +233,49 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
                              _ptr(lse), _ptr(ez), _ptr(g_loss), _ptr(g_entropy), _ptr(dh),
                              _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)))
     return dh, dw
+
+
+def flce_shard_stats(hidden, weight, labels, v_offset, v_total, softcap=0.0,
+                     ignore_index=IGNORE_INDEX, weight_layout="hv", validate=False,
+                     workspace=None, stream=None, out=None):
+    """Statistics [4, N] fp32 of one vocabulary shard (columns [v_offset, v_offset + V)
+    of v_total); see flce.h for their meaning."""
+    lib = load_library()
+    N, H, V, wshape = _dims(hidden, weight, weight_layout)
+    _need(hidden, "hidden", torch.bfloat16, (N, H))
+    _need(weight, "weight", torch.bfloat16, wshape)
+    _need(labels, "labels", torch.int64, (N,))
+    p = make_params(N, H, V, "none", ignore_index, 0.0, softcap, validate,
+                    weight_layout=weight_layout, v_offset=v_offset, v_total=v_total)
+    stats = out if out is not None else torch.empty(4, N, dtype=torch.float32,
+                                                    device=hidden.device)
+    ws = _workspace(p, 0, hidden.device, workspace)
+    _check(lib.flce_shard_stats(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
+                                _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)))
+    return stats
+
+
+def flce_combine_shards(stats, labels, v_total, reduction="mean", ignore_index=IGNORE_INDEX,
+                        zloss_coef=0.0, H=8, validate=False, workspace=None, stream=None):
+    """Merge [P, 4, N] shard statistics into (loss, entropy, lse, ez) for the whole
+    vocabulary of v_total entries."""
+    lib = load_library()
+    P, four, N = stats.shape
+    _need(stats, "stats", torch.float32, (P, 4, N))
+    _need(labels, "labels", torch.int64, (N,))
+    p = make_params(N, H, v_total, reduction, ignore_index, zloss_coef, 0.0, validate,
+                    v_offset=0, v_total=v_total)
+    dev = stats.device
+    n_out = N if p.reduction == RED_NONE else 1
+    loss = torch.empty(n_out, dtype=torch.float32, device=dev)
+    ent = torch.empty(n_out, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    ez = torch.empty(N, dtype=torch.float32, device=dev)
+    ws = _workspace(p, 2, dev, workspace)
+    _check(lib.flce_combine_shards(ctypes.byref(p), _ptr(stats), P, _ptr(labels), _ptr(loss),
+                                   _ptr(ent), _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
+                                   _stream(stream)))
+    return loss, ent, lse, ez
 
 
 def flce_status(workspace, stream=None) -> int:

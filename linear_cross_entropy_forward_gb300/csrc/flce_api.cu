@@ -57,38 +57,57 @@ struct Smoothing {
   const float* wsum;  // device scalar (NULL: V, all weights 1)
 };
 
+// Partial statistics to merge per row: part p of row n holds (m, d, s) at
+// offset p * part_stride + n of pm / pd / ps.  The label logit comes from
+// zlabel[n], or, when pzy is set (vocabulary shards), is the sum over the parts of
+// pzy[p * part_stride + n] (the one shard that holds the label contributes it).
+struct Parts {
+  const float* pm;
+  const float* pd;
+  const float* ps;
+  const float* pzy;
+  int64_t n_parts;
+  int64_t part_stride;
+};
+
+// Merges the parts of 32 rows per block (8 warps over the parts) and finalises:
+// lse, E_p[z], CE (+ smoothing / class weights), z-loss, entropy, ignore mask.
+// V is the whole vocabulary (labels outside [0, V) that are not ignored are errors).
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
-    const float* __restrict__ pm, const float* __restrict__ pd, const float* __restrict__ ps,
-    int64_t n_parts, int64_t N, const float* __restrict__ zlabel,
-    const int64_t* __restrict__ labels, int64_t V, int64_t ignore_index, float zcoef,
-    Smoothing sm, float* __restrict__ lse_out, float* __restrict__ ez_out,
-    float* __restrict__ loss_row, float* __restrict__ ent_row, uint32_t* err) {
-  __shared__ float sM[8][32], sD[8][32], sS[8][32], sW[8][32];
+    Parts pt, int64_t N, const float* __restrict__ zlabel, const int64_t* __restrict__ labels,
+    int64_t V, int64_t ignore_index, float zcoef, Smoothing sm, float* __restrict__ lse_out,
+    float* __restrict__ ez_out, float* __restrict__ loss_row, float* __restrict__ ent_row,
+    uint32_t* err) {
+  __shared__ float sM[8][32], sD[8][32], sS[8][32], sW[8][32], sZ[8][32];
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   const bool smooth = sm.eps != 0.0f;
-  float M = -1e30f, D = 0.0f, S = 0.0f, SW = 0.0f;
+  float M = -1e30f, D = 0.0f, S = 0.0f, SW = 0.0f, ZY = 0.0f;
   if (n < N) {
-    for (int64_t p = w; p < n_parts; p += 8) {
-      const int64_t o = p * N + n;
-      merge_stats(M, D, S, pm[o], pd[o], ps[o]);
+    for (int64_t p = w; p < pt.n_parts; p += 8) {
+      const int64_t o = p * pt.part_stride + n;
+      merge_stats(M, D, S, pt.pm[o], pt.pd[o], pt.ps[o]);
       if (smooth) SW += sm.psw[o];
+      if (pt.pzy) ZY += pt.pzy[o];
     }
   }
   sM[w][lane] = M;
   sD[w][lane] = D;
   sS[w][lane] = S;
   sW[w][lane] = SW;
+  sZ[w][lane] = ZY;
   __syncthreads();
   if (w != 0 || n >= N) return;
   M = sM[0][lane];
   D = sD[0][lane];
   S = sS[0][lane];
   SW = sW[0][lane];
+  ZY = sZ[0][lane];
   for (int k = 1; k < 8; ++k) {
     merge_stats(M, D, S, sM[k][lane], sD[k][lane], sS[k][lane]);
     SW += sW[k][lane];
+    ZY += sZ[k][lane];
   }
   // M, S in log2 units: lse = ln2 (M + log2 D); entropy = ln d - s_c/d = ln2 (log2 D - S/D)
   const float l2d = log2f(D);
@@ -103,7 +122,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(
       atomicOr(err, FLCE_DEVERR_LABEL);
       lt = et = __int_as_float(0x7fc00000);
     } else {
-      float ce = lse - zlabel[n];
+      float ce = lse - (pt.pzy ? ZY : zlabel[n]);
       if (smooth || sm.cw) {
         // (1 - eps) w_y (lse - z_y) + eps/V (W lse - sum_v w_v z_v)
         const float wy = sm.cw ? sm.cw[y] : 1.0f;
@@ -191,6 +210,37 @@ __global__ void __launch_bounds__(1024) class_weight_sum_kernel(const float* __r
     __syncthreads();
   }
   if (threadIdx.x == 0) wsum[0] = static_cast<float>(sw[0]);
+}
+
+// One vocabulary shard's statistics per row, [4, N]: the merge of its column
+// parts (m, d, s in log2 units) and the label logit if the label is in the shard.
+__global__ void __launch_bounds__(256) shard_stats_kernel(
+    const float* __restrict__ pm, const float* __restrict__ pd, const float* __restrict__ ps,
+    int64_t n_parts, int64_t N, const float* __restrict__ zlabel,
+    const int64_t* __restrict__ labels, int64_t v_offset, int64_t v_shard,
+    float* __restrict__ stats) {
+  __shared__ float sM[8][32], sD[8][32], sS[8][32];
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  float M = -1e30f, D = 0.0f, S = 0.0f;
+  if (n < N)
+    for (int64_t p = w; p < n_parts; p += 8) merge_stats(M, D, S, pm[p * N + n], pd[p * N + n],
+                                                         ps[p * N + n]);
+  sM[w][lane] = M;
+  sD[w][lane] = D;
+  sS[w][lane] = S;
+  __syncthreads();
+  if (w != 0 || n >= N) return;
+  M = sM[0][lane];
+  D = sD[0][lane];
+  S = sS[0][lane];
+  for (int k = 1; k < 8; ++k) merge_stats(M, D, S, sM[k][lane], sD[k][lane], sS[k][lane]);
+  const int64_t y = labels[n] - v_offset;
+  stats[n] = M;
+  stats[N + n] = D;
+  stats[2 * N + n] = S;
+  stats[3 * N + n] = (y >= 0 && y < v_shard) ? zlabel[n] : 0.0f;
 }
 
 // Per-row constants of the dlogits epilogue, with a_ce / a_z / b the upstream
@@ -333,6 +383,12 @@ int check_params(const flce_params* p) {
   if (p->weight_layout != FLCE_WEIGHT_HV && p->weight_layout != FLCE_WEIGHT_VH)
     return FLCE_ERR_BAD_ARG;
   if (!(p->label_smoothing >= 0.0f && p->label_smoothing <= 1.0f)) return FLCE_ERR_BAD_ARG;
+  if (p->v_total < 0 || p->v_offset < 0) return FLCE_ERR_BAD_ARG;
+  if (p->v_total == 0 && p->v_offset != 0) return FLCE_ERR_BAD_ARG;
+  if (p->v_total > 0) {
+    if (p->v_offset + p->V > p->v_total || p->v_total > kMaxDim) return FLCE_ERR_BAD_SHAPE;
+    if (p->label_smoothing != 0.0f || p->class_weight) return FLCE_ERR_BAD_ARG;
+  }
   if (reinterpret_cast<uintptr_t>(p->class_weight) & 3) return FLCE_ERR_ALIGN;
   // chunk-relative and vocabulary column indices are 32-bit inside the kernels
   if (cdiv(p->V, 256) * 256 > kMaxDim) return FLCE_ERR_BAD_SHAPE;
@@ -472,14 +528,25 @@ size_t flce_workspace_size(const flce_params* p, int phase) {
   if (check_params(p) != FLCE_OK) return 0;
   if (phase == 0) return fwd_layout(p).total;
   if (phase == 1) return bwd_layout(p).total;
+  if (phase == 2) return kHeaderBytes + 2 * align256(static_cast<size_t>(p->N) * 4);
   return 0;
 }
 
 int flce_kernel_launches(const flce_params* p, int phase) {
   if (check_params(p) != FLCE_OK || p->N == 0) return check_params(p) != FLCE_OK ? -1 : 0;
-  if (phase == 0) return p->reduction == FLCE_RED_NONE ? 2 : 3;
-  if (phase == 1) return 1 + 3 * static_cast<int>(bwd_layout(p).chunks);
-  return -1;
+  const int reduce = p->reduction == FLCE_RED_NONE ? 0 : 1;
+  switch (phase) {
+    case 0:  // flce_forward: GEMM, [class-weight sum], combine, [reduce]
+      return 2 + reduce + (p->label_smoothing != 0.0f && p->class_weight ? 1 : 0);
+    case 1:  // flce_backward: prep + 3 GEMMs per vocabulary chunk
+      return 1 + 3 * static_cast<int>(bwd_layout(p).chunks);
+    case 2:  // flce_combine_shards: combine, [reduce]
+      return 1 + reduce;
+    case 3:  // flce_shard_stats: GEMM, shard merge
+      return 2;
+    default:
+      return -1;
+  }
 }
 
 int flce_status(const void* workspace, void* stream) {
@@ -487,36 +554,17 @@ int flce_status(const void* workspace, void* stream) {
   return read_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
-int flce_forward(const flce_params* p, const void* hidden, const void* weight,
-                 const int64_t* labels, float* loss, float* entropy, float* lse, float* ez,
-                 void* workspace, size_t ws_bytes, void* stream) {
-  int rc = check_params(p);
-  if (rc) return rc;
-  if (!loss || !entropy || !workspace || !weight) return FLCE_ERR_BAD_ARG;
-  if (p->N > 0 && (!hidden || !labels || !lse || !ez)) return FLCE_ERR_BAD_ARG;
-  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(loss) ||
-      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255))
-    return FLCE_ERR_ALIGN;
-  const FwdLayout L = fwd_layout(p);
-  if (ws_bytes < L.total) return FLCE_ERR_WS_TOO_SMALL;
-  DevInfo di;
-  if ((rc = device_info(&di))) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-  if ((rc = cuda_rc(cudaMemsetAsync(ws, 0, kHeaderBytes, st)))) return rc;
-  const bool per_token = p->reduction == FLCE_RED_NONE;
+}  // extern "C"
+
+namespace flce {
+namespace {
+
+// Stage 1 of the forward: logits tiles of hidden @ weight reduced to per-row,
+// per-column-block online-softmax partials (and the label logit) in the workspace.
+int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
+                  const int64_t* labels, uint8_t* ws, const FwdLayout& L, uint32_t* err,
+                  cudaStream_t st, EpiArgs* ea_out) {
   const int64_t N = p->N, H = p->H, V = p->V;
-
-  if (N == 0) {
-    if (!per_token) {
-      if ((rc = cuda_rc(cudaMemsetAsync(loss, 0, 4, st)))) return rc;
-      if ((rc = cuda_rc(cudaMemsetAsync(entropy, 0, 4, st)))) return rc;
-    }
-    return p->validate ? read_status(ws, st) : FLCE_OK;
-  }
-
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, hidden, H, N, H, BK, 128)) return FLCE_ERR_CUDA;
@@ -538,6 +586,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   ea.V = V;
   ea.softcap = p->softcap;
   ea.labels = labels;
+  ea.label_offset = p->v_offset;
   ea.ignore_index = p->ignore_index;
   ea.pm = reinterpret_cast<float*>(ws + L.pm);
   ea.pd = reinterpret_cast<float*>(ws + L.pd);
@@ -548,28 +597,144 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
   ea.cw = p->class_weight;
   ea.psw = reinterpret_cast<float*>(ws + L.psw);
   ea.err = err;
-  if ((rc = cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st))))
-    return rc;
+  *ea_out = ea;
+  return cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st));
+}
+
+// Stage 2: per-row outputs from the merged parts, then the reduction over rows.
+int run_fwd_finish(const flce_params* p, const Parts& pt, const float* zlabel,
+                   const int64_t* labels, const Smoothing& sm, float* loss, float* entropy,
+                   float* lse, float* ez, uint8_t* ws, size_t loss_row_off, size_t ent_row_off,
+                   uint32_t* err, cudaStream_t st) {
+  const int64_t N = p->N;
+  const int64_t V_all = p->v_total > 0 ? p->v_total : p->V;
+  const bool per_token = p->reduction == FLCE_RED_NONE;
+  float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + loss_row_off);
+  float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + ent_row_off);
+  fwd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 32)), 256, 0, st>>>(
+      pt, N, zlabel, labels, V_all, p->ignore_index, p->zloss_coef, sm, lse, ez, loss_row,
+      ent_row, err);
+  int rc = cuda_rc(cudaGetLastError());
+  if (rc || per_token) return rc;
+  reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,
+                                         p->reduction == FLCE_RED_MEAN, p->class_weight, lse,
+                                         p->zloss_coef, loss, entropy);
+  return cuda_rc(cudaGetLastError());
+}
+
+// Common entry checks and workspace header reset; returns the status and, on
+// success, the stream and the error word.
+int begin_call(const void* workspace, size_t ws_bytes, size_t need, void* stream,
+               cudaStream_t* st, uint32_t** err) {
+  if (ws_bytes < need) return FLCE_ERR_WS_TOO_SMALL;
+  DevInfo di;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  *st = static_cast<cudaStream_t>(stream);
+  *err = static_cast<uint32_t*>(const_cast<void*>(workspace));
+  return cuda_rc(cudaMemsetAsync(const_cast<void*>(workspace), 0, kHeaderBytes, *st));
+}
+
+int zero_reduced(const flce_params* p, float* loss, float* entropy, cudaStream_t st) {
+  if (p->reduction == FLCE_RED_NONE) return FLCE_OK;
+  int rc = cuda_rc(cudaMemsetAsync(loss, 0, 4, st));
+  return rc ? rc : cuda_rc(cudaMemsetAsync(entropy, 0, 4, st));
+}
+
+}  // namespace
+}  // namespace flce
+
+extern "C" {
+
+int flce_forward(const flce_params* p, const void* hidden, const void* weight,
+                 const int64_t* labels, float* loss, float* entropy, float* lse, float* ez,
+                 void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  // a shard's softmax is not the whole vocabulary's: shards use flce_shard_stats
+  if (p->v_total > 0 && !(p->v_offset == 0 && p->v_total == p->V)) return FLCE_ERR_BAD_ARG;
+  if (!loss || !entropy || !workspace || !weight) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!hidden || !labels || !lse || !ez)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(loss) ||
+      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const FwdLayout L = fwd_layout(p);
+  cudaStream_t st;
+  uint32_t* err;
+  if ((rc = begin_call(workspace, ws_bytes, L.total, stream, &st, &err))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p->N == 0) {
+    if ((rc = zero_reduced(p, loss, entropy, st))) return rc;
+    return p->validate ? read_status(ws, st) : FLCE_OK;
+  }
+  EpiArgs ea;
+  if ((rc = run_fwd_stats(p, hidden, weight, labels, ws, L, err, st, &ea))) return rc;
   Smoothing sm{p->label_smoothing, p->class_weight, ea.psw, nullptr};
   if (p->label_smoothing != 0.0f && p->class_weight) {
     float* wsum = reinterpret_cast<float*>(ws + kWsumOffset);
-    class_weight_sum_kernel<<<1, 1024, 0, st>>>(p->class_weight, V, wsum);
+    class_weight_sum_kernel<<<1, 1024, 0, st>>>(p->class_weight, p->V, wsum);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
     sm.wsum = wsum;
   }
+  const Parts pt{ea.pm, ea.pd, ea.ps, nullptr, L.n_parts, p->N};
+  if ((rc = run_fwd_finish(p, pt, ea.zlabel, labels, sm, loss, entropy, lse, ez, ws,
+                           L.loss_row, L.ent_row, err, st)))
+    return rc;
+  return p->validate ? read_status(ws, st) : FLCE_OK;
+}
 
-  float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
-  float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
-  fwd_combine_kernel<<<static_cast<unsigned>(cdiv(N, 32)), 256, 0, st>>>(
-      ea.pm, ea.pd, ea.ps, L.n_parts, N, ea.zlabel, labels, V, p->ignore_index, p->zloss_coef,
-      sm, lse, ez, loss_row, ent_row, err);
-  if ((rc = cuda_rc(cudaGetLastError()))) return rc;
-  if (!per_token) {
-    reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,
-                                           p->reduction == FLCE_RED_MEAN, p->class_weight,
-                                           lse, p->zloss_coef, loss, entropy);
+int flce_shard_stats(const flce_params* p, const void* hidden, const void* weight,
+                     const int64_t* labels, float* stats, void* workspace, size_t ws_bytes,
+                     void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!stats || !workspace || !weight) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!hidden || !labels)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(stats) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const FwdLayout L = fwd_layout(p);
+  cudaStream_t st;
+  uint32_t* err;
+  if ((rc = begin_call(workspace, ws_bytes, L.total, stream, &st, &err))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p->N > 0) {
+    EpiArgs ea;
+    if ((rc = run_fwd_stats(p, hidden, weight, labels, ws, L, err, st, &ea))) return rc;
+    shard_stats_kernel<<<static_cast<unsigned>(cdiv(p->N, 32)), 256, 0, st>>>(
+        ea.pm, ea.pd, ea.ps, L.n_parts, p->N, ea.zlabel, labels, p->v_offset, p->V, stats);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
   }
+  return p->validate ? read_status(ws, st) : FLCE_OK;
+}
+
+int flce_combine_shards(const flce_params* p, const float* stats, int32_t n_shards,
+                        const int64_t* labels, float* loss, float* entropy, float* lse,
+                        float* ez, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (n_shards < 1 || !loss || !entropy || !workspace) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!stats || !labels || !lse || !ez)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(stats) || !aligned16(labels) || !aligned16(loss) || !aligned16(entropy) ||
+      !aligned16(lse) || !aligned16(ez) || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
+  cudaStream_t st;
+  uint32_t* err;
+  if ((rc = begin_call(workspace, ws_bytes, kHeaderBytes + 2 * row_bytes, stream, &st, &err)))
+    return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (p->N == 0) {
+    if ((rc = zero_reduced(p, loss, entropy, st))) return rc;
+    return p->validate ? read_status(ws, st) : FLCE_OK;
+  }
+  const int64_t N = p->N;
+  const Parts pt{stats, stats + N, stats + 2 * N, stats + 3 * N, n_shards, 4 * N};
+  const Smoothing sm{0.0f, nullptr, nullptr, nullptr};
+  if ((rc = run_fwd_finish(p, pt, nullptr, labels, sm, loss, entropy, lse, ez, ws, kHeaderBytes,
+                           kHeaderBytes + row_bytes, err, st)))
+    return rc;
   return p->validate ? read_status(ws, st) : FLCE_OK;
 }
 
@@ -649,6 +814,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e3.V = V;
     e3.softcap = p->softcap;
     e3.labels = labels;
+    e3.label_offset = p->v_offset;
     e3.ignore_index = p->ignore_index;
     e3.rowc = rowc;
     e3.rowd = rowd;

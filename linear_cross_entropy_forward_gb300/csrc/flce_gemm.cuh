@@ -98,6 +98,7 @@ struct EpiArgs {
   int64_t V;           // vocabulary size (masking of the softmax)
   float softcap;       // 0 = off
   const int64_t* labels;
+  int64_t label_offset;  // vocabulary index of problem column 0's shard (0 unsharded)
   int64_t ignore_index;
   // EPI_FWD_STATS
   float* pm;
@@ -173,7 +174,7 @@ struct Epilogue<EPI_FWD_STATS> {
     const bool row_ok = row < ea.rows;
     int y = -1;
     if (row_ok) {
-      int64_t yl = ea.labels[row];
+      const int64_t yl = ea.labels[row] - ea.label_offset;
       if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
     }
     const bool cap = ea.softcap != 0.0f;
@@ -259,7 +260,7 @@ struct Epilogue<EPI_DLOGITS> {
     if (row_ok) {
       rc = ea.rowc[row];
       if (smooth) dcoef = ea.rowd[row];
-      int64_t yl = ea.labels[row];
+      const int64_t yl = ea.labels[row] - ea.label_offset;
       if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
     }
     const bool cap = ea.softcap != 0.0f;

@@ -3,6 +3,6 @@
 TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
 benchmark's CPU-baseline leg, never by the product path.
 """
-from .flce_oracle import (IGNORE_INDEX, backward, bf16_bits_to_f64, dlogits_chunk,  # noqa: F401
-                          forward, grad_scales, label_logits, logits_chunk, objective,
-                          row_stats)
+from .flce_oracle import (IGNORE_INDEX, backward, bf16_bits_to_f64, combine_shards,  # noqa: F401
+                          dlogits_chunk, forward, grad_scales, label_logits, logits_chunk,
+                          objective, row_stats, shard_stats)

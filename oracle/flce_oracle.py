@@ -76,7 +76,7 @@ def _class_weights(class_weight, V):
     return w
 
 
-def _check(hidden, weight, labels, reduction, ignore_index):
+def _check(hidden, weight, labels, reduction, ignore_index, v_total=None):
     if reduction not in _REDS:
         raise ValueError(f"reduction must be one of {_REDS}")
     N, H = hidden.shape
@@ -85,7 +85,7 @@ def _check(hidden, weight, labels, reduction, ignore_index):
         raise ValueError("shape mismatch")
     lab = np.asarray(labels, dtype=np.int64)
     valid = lab != ignore_index
-    if np.any((lab[valid] < 0) | (lab[valid] >= V)):
+    if np.any((lab[valid] < 0) | (lab[valid] >= (V if v_total is None else v_total))):
         raise ValueError("label out of range")
     return N, H, V, lab, valid
 
@@ -198,16 +198,19 @@ def grad_scales(g_loss, g_entropy, valid, reduction, w_valid=None):
 
 
 def dlogits_chunk(hidden, weight, labels, lse, ez, gc, gl, ge, v0, v1,
-                  zloss_coef=0.0, softcap=0.0, label_smoothing=0.0, class_weight=None):
+                  zloss_coef=0.0, softcap=0.0, label_smoothing=0.0, class_weight=None,
+                  v_offset=0):
     """Gradient of the objective w.r.t. the raw (pre-cap) logits z'[:, v0:v1]
     (gc, gl, ge: per-row scaled upstream grads of the cross-entropy part, the
-    z-loss part and the entropy, from grad_scales)."""
+    z-loss part and the entropy, from grad_scales).  Column v of weight is the
+    vocabulary entry v_offset + v (a vocabulary shard)."""
     V = weight.shape[1]
     cw = _class_weights(class_weight, V)
     eps = float(label_smoothing)
     z = logits_chunk(hidden, weight, v0, v1, softcap)
     p = np.exp(z - lse[:, None])
-    onehot = (labels[:, None] == np.arange(v0, v1)[None, :]).astype(np.float64)
+    onehot = (labels[:, None] == np.arange(v_offset + v0, v_offset + v1)[None, :]
+              ).astype(np.float64)
     wy = cw[np.clip(labels, 0, V - 1)][:, None]
     ce_grad = p * ((1.0 - eps) * wy + eps * cw.sum() / V) - (1.0 - eps) * wy * onehot \
         - (eps / V) * cw[v0:v1][None, :]
@@ -220,21 +223,26 @@ def dlogits_chunk(hidden, weight, labels, lse, ez, gc, gl, ge, v0, v1,
 
 def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, v_chunk=8192,
-             rows=None, label_smoothing=0.0, class_weight=None):
+             rows=None, label_smoothing=0.0, class_weight=None, v_offset=0, v_total=None):
     """(dhidden, dweight) in fp64.
 
     ``lse``/``ez`` must come from :func:`forward` on the same inputs.  With
     ``rows`` given, only dhidden[rows] is formed (dweight is then None): each
-    dhidden row needs only its own row of the logits.
+    dhidden row needs only its own row of the logits.  With a vocabulary shard
+    (weight = columns [v_offset, v_offset + V) of v_total, lse / ez of the whole
+    vocabulary) the result is the shard's dweight and its term of dhidden.
     """
     hidden = np.asarray(hidden, dtype=np.float64)
     weight = np.asarray(weight, dtype=np.float64)
-    N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
+    N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index, v_total)
+    if v_total is not None and (label_smoothing != 0.0 or class_weight is not None):
+        raise ValueError("vocabulary shards exclude label smoothing and class weights")
     cw = _class_weights(class_weight, V)
-    w_valid = float(np.where(valid, cw[np.where(valid, lab, 0)], 0.0).sum())
+    w_valid = float(np.where(valid, cw[np.where(valid, lab, 0)], 0.0).sum()) \
+        if class_weight is not None else float(valid.sum())
     gc, gl, ge = grad_scales(g_loss, g_entropy, valid, reduction, w_valid)
     opts = dict(zloss_coef=zloss_coef, softcap=softcap, label_smoothing=label_smoothing,
-                class_weight=class_weight)
+                class_weight=class_weight, v_offset=v_offset)
     if rows is not None:
         rows = np.asarray(rows, dtype=np.int64)
         hs, ls, vs = hidden[rows], lab[rows], valid[rows]
@@ -268,3 +276,67 @@ def objective(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
         return float(np.dot(gl * np.ones_like(out["loss"]), out["loss"])
                      + np.dot(ge * np.ones_like(out["entropy"]), out["entropy"]))
     return float(gl[0] * out["loss"] + ge[0] * out["entropy"])
+
+
+# --------------------------------------------------------------------------- vocabulary shards
+def shard_stats(hidden, weight, labels, v_offset, softcap=0.0, v_chunk=8192):
+    """Softmax statistics of one vocabulary shard (weight = columns [v_offset, v_offset + V)
+    of the whole vocabulary), two passes: m = max z, d = sum exp(z - m),
+    s = sum exp(z - m) z, and the label's logit z_y when the label is in the shard
+    (0 otherwise).  Returns a (4, N) array."""
+    hidden = np.asarray(hidden, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    lab = np.asarray(labels, dtype=np.int64)
+    V = weight.shape[1]
+    m = np.full(hidden.shape[0], -np.inf)
+    for v0 in range(0, V, v_chunk):
+        m = np.maximum(m, logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap).max(1))
+    d = np.zeros(hidden.shape[0])
+    s = np.zeros(hidden.shape[0])
+    for v0 in range(0, V, v_chunk):
+        z = logits_chunk(hidden, weight, v0, min(V, v0 + v_chunk), softcap)
+        e = np.exp(z - m[:, None])
+        d += e.sum(1)
+        s += (e * z).sum(1)
+    inside = (lab >= v_offset) & (lab < v_offset + V)
+    zy = np.zeros(hidden.shape[0])
+    idx = np.nonzero(inside)[0]
+    if idx.size:
+        zy[idx] = _cap(np.einsum("nh,hn->n", hidden[idx], weight[:, lab[idx] - v_offset]),
+                       softcap)
+    return np.stack([m, d, s, zy])
+
+
+def combine_shards(stats, labels, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
+                   v_total=None):
+    """Whole-vocabulary loss / entropy / lse / E_p[z] from the (P, 4, N) statistics of P
+    shards: M = max_p m_p, D = sum_p d_p exp(m_p - M), S = sum_p s_p exp(m_p - M)
+    (the online-softmax merge of Liger-Kernel PR #551's first pass), lse = M + log D,
+    E_p[z] = S / D, z_y = sum_p z_y,p."""
+    st = np.asarray(stats, dtype=np.float64)
+    lab = np.asarray(labels, dtype=np.int64)
+    if reduction not in _REDS:
+        raise ValueError(f"reduction must be one of {_REDS}")
+    M = st[:, 0].max(axis=0)
+    scale = np.exp(st[:, 0] - M[None, :])
+    D = (st[:, 1] * scale).sum(0)
+    S = (st[:, 2] * scale).sum(0)
+    zy = st[:, 3].sum(0)
+    lse = M + np.log(D)
+    ez = S / D
+    valid = lab != ignore_index
+    if v_total is not None and np.any((lab[valid] < 0) | (lab[valid] >= v_total)):
+        raise ValueError("label out of range")
+    ce = np.where(valid, lse - zy, 0.0)
+    ent = np.where(valid, lse - ez, 0.0)
+    loss_tok = ce + np.where(valid, zloss_coef * lse * lse, 0.0)
+    n_valid = int(valid.sum())
+    if reduction == "none":
+        loss, entropy = loss_tok, ent
+    elif reduction == "sum":
+        loss, entropy = float(loss_tok.sum()), float(ent.sum())
+    else:
+        loss = float(loss_tok.sum()) / n_valid if n_valid else 0.0
+        entropy = float(ent.sum()) / n_valid if n_valid else 0.0
+    return dict(loss=loss, entropy=entropy, loss_tok=loss_tok, entropy_tok=ent, lse=lse, ez=ez,
+                valid=valid, n_valid=n_valid)

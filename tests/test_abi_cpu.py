@@ -42,12 +42,33 @@ def test_version_and_strerror(lib):
 
 
 def test_params_struct_layout():
-    # int64 x4, int32, float, float, int32, int64, int32, float, pointer -> 72 bytes (flce.h)
-    assert ctypes.sizeof(B.FlceParams) == 72
+    # int64 x4, int32, float, float, int32, int64, int32, float, pointer, int64 x2
+    # -> 88 bytes, as in flce.h
+    assert ctypes.sizeof(B.FlceParams) == 88
     assert B.FlceParams.chunk_v.offset == 48
     assert B.FlceParams.weight_layout.offset == 56
     assert B.FlceParams.label_smoothing.offset == 60
     assert B.FlceParams.class_weight.offset == 64
+    assert B.FlceParams.v_offset.offset == 72
+    assert B.FlceParams.v_total.offset == 80
+
+
+def test_params_struct_matches_the_c_compiler(tmp_path):
+    """sizeof / offsetof of flce_params from the C compiler agree with the binding."""
+    import subprocess
+    src = tmp_path / "t.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "flce.h"\n'
+        'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(flce_params),'
+        ' offsetof(flce_params, chunk_v), offsetof(flce_params, class_weight),'
+        ' offsetof(flce_params, v_offset), offsetof(flce_params, v_total)); return 0;}\n')
+    exe = tmp_path / "t"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    F = B.FlceParams
+    assert [int(x) for x in out] == [ctypes.sizeof(F), F.chunk_v.offset, F.class_weight.offset,
+                                     F.v_offset.offset, F.v_total.offset]
 
 
 def test_workspace_sizes(lib):
@@ -76,6 +97,9 @@ def test_workspace_sizes(lib):
     (dict(N=10, H=64, V=64, weight_layout=7), 1),
     (dict(N=10, H=64, V=64, label_smoothing=1.5), 1),
     (dict(N=10, H=64, V=64, label_smoothing=-0.1), 1),
+    (dict(N=10, H=64, V=64, v_offset=8), 1),                  # offset without a total
+    (dict(N=10, H=64, V=64, v_offset=8, v_total=64), 2),      # shard past the vocabulary
+    (dict(N=10, H=64, V=64, v_total=128, label_smoothing=0.1), 1),
 ])
 def test_bad_params_rejected_on_host(lib, kw, code):
     args = dict(N=10, H=64, V=64)

@@ -1,0 +1,113 @@
+"""Vocabulary-parallel path on one GPU: the shards run one after another through
+flce_shard_stats -> flce_combine_shards -> flce_backward (per shard) and must match the
+whole-vocabulary fp64 oracle (tolerances as in the other parity tests); the
+single-rank autograd wrapper must match the unsharded entry points."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_forward_gb300 import (flce_backward, flce_combine_shards,
+                                                flce_forward, flce_shard_stats,
+                                                vocab_parallel_linear_cross_entropy)
+from linear_cross_entropy_forward_gb300 import workloads as wl
+from oracle import flce_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+TOK_ABS = 2e-3
+RED_REL = 1e-4
+GRAD_REL_L2 = 1e-2
+
+
+def _cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_cross_entropy_forward_gb300.build import build
+    build()
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+CASES = [
+    ("none_3shards", dataclasses.replace(wl.TINY, name="vp1", N=300, H=200, V=1000,
+                                         reduction="none", grad_mode="normal"),
+     [0, 256, 648, 1000], "hv"),
+    ("mean_zloss_cap", dataclasses.replace(wl.TINY, name="vp2", N=384, H=256, V=2048, w_std=0.2,
+                                           zloss_coef=1e-3, softcap=4.0),
+     [0, 1024, 2048], "hv"),
+    ("sum_vh_4shards", dataclasses.replace(wl.TINY, name="vp3", N=260, H=128, V=776,
+                                           reduction="sum"),
+     [0, 200, 392, 584, 776], "vh"),
+]
+
+
+@pytest.mark.parametrize("name,w,cuts,layout", CASES, ids=[c[0] for c in CASES])
+def test_sequential_shards_match_oracle(name, w, cuts, layout):
+    _cuda_or_skip()
+    dev = torch.device("cuda")
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    hd, yd = hidden.to(dev), labels.to(dev)
+    shards = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        ws = weight[:, a:b]
+        shards.append((a, (ws if layout == "hv" else ws.t()).contiguous().to(dev)))
+    stats = torch.stack([flce_shard_stats(hd, ws, yd, a, w.V, softcap=w.softcap,
+                                          weight_layout=layout, validate=True)
+                         for a, ws in shards])
+    loss, ent, lse, ez = flce_combine_shards(stats, yd, w.V, w.reduction,
+                                             zloss_coef=w.zloss_coef, H=w.H, validate=True)
+    dh = torch.zeros(w.N, w.H, device=dev)
+    dws = []
+    for a, ws in shards:
+        dhp, dwp = flce_backward(hd, ws, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
+                                 zloss_coef=w.zloss_coef, softcap=w.softcap, validate=True,
+                                 weight_layout=layout, v_offset=a, v_total=w.V)
+        dh += dhp.float()
+        dws.append(dwp if layout == "hv" else dwp.t())
+    dw = torch.cat(dws, dim=1)
+    torch.cuda.synchronize()
+
+    h64 = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
+    W64 = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
+    y = labels.numpy()
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+    o = orc.forward(h64, W64, y, w.reduction, **kw)
+    dh_o, dw_o = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.numpy(), g_ent.numpy(),
+                              w.reduction, **kw)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    assert np.abs(f(lse) - o["lse"]).max() <= TOK_ABS
+    assert np.abs(f(ez) - o["ez"]).max() <= TOK_ABS
+    if w.reduction == "none":
+        assert np.abs(f(loss) - o["loss"]).max() <= TOK_ABS
+        assert np.abs(f(ent) - o["entropy"]).max() <= TOK_ABS
+    else:
+        assert abs(loss.item() - o["loss"]) <= RED_REL * abs(o["loss"])
+        assert abs(ent.item() - o["entropy"]) <= RED_REL * abs(o["entropy"])
+    assert rel_l2(f(dh), dh_o) <= GRAD_REL_L2
+    assert rel_l2(f(dw), dw_o) <= GRAD_REL_L2
+
+
+def test_single_rank_wrapper_matches_unsharded_path():
+    """Without a process group the wrapper is one shard holding the whole vocabulary:
+    the same numbers as flce_forward / flce_backward."""
+    _cuda_or_skip()
+    dev = torch.device("cuda")
+    w = dataclasses.replace(wl.TINY, name="vp4", N=256, H=128, V=1024, zloss_coef=1e-3)
+    hidden, weight, labels, _, _ = wl.make_inputs(w)
+    h = hidden.to(dev).requires_grad_(True)
+    W = weight.to(dev).requires_grad_(True)
+    y = labels.to(dev)
+    loss, ent = vocab_parallel_linear_cross_entropy(h, W, y, 0, w.V, "mean", zloss_coef=1e-3)
+    (loss + 0.25 * ent).backward()
+    ref = flce_forward(h.detach(), W.detach(), y, "mean", zloss_coef=1e-3)
+    assert abs(loss.item() - ref[0].item()) <= 1e-5 * abs(ref[0].item())
+    assert abs(ent.item() - ref[1].item()) <= 1e-5 * abs(ref[1].item())
+    dh, dw = flce_backward(h.detach(), W.detach(), y, ref[2], ref[3],
+                           torch.ones(1, device=dev), torch.full((1,), 0.25, device=dev),
+                           "mean", zloss_coef=1e-3)
+    assert rel_l2(h.grad.float().cpu().numpy(), dh.float().cpu().numpy()) <= 1e-3
+    assert rel_l2(W.grad.float().cpu().numpy(), dw.float().cpu().numpy()) <= 1e-3

@@ -383,3 +383,34 @@ def test_uniform_class_weights_scale_out_of_the_mean():
     d = orc.forward(hidden, weight, labels, "sum", label_smoothing=0.1,
                     class_weight=np.full(30, 3.0))
     np.testing.assert_allclose(d["loss"], 3.0 * c["loss"], rtol=1e-12)
+
+
+# --------------------------------------------------------------------------- vocabulary shards
+@pytest.mark.parametrize("reduction", REDS)
+@pytest.mark.parametrize("cap", [0.0, 2.0])
+def test_shard_merge_equals_whole_vocabulary(reduction, cap):
+    """Splitting the vocabulary anywhere and merging the shards' (m, d, s, z_y) gives the
+    whole-vocabulary results; each shard's backward sums to the whole backward."""
+    N, H, V = 23, 9, 61
+    hidden, weight, labels = _rand_case(N, H, V, 80, w_std=1.2, ignore=(3, 11))
+    whole = orc.forward(hidden, weight, labels, reduction, zloss_coef=0.02, softcap=cap)
+    gl, ge = _grads(reduction, N, 80)
+    dh_w, dw_w = orc.backward(hidden, weight, labels, whole["lse"], whole["ez"], gl, ge,
+                              reduction, zloss_coef=0.02, softcap=cap)
+    for cuts in ([0, V], [0, 1, V], [0, 20, 21, 44, V], list(range(0, V + 1, 7)) + [V]):
+        cuts = sorted(set(cuts))
+        st = np.stack([orc.shard_stats(hidden, weight[:, a:b], labels, a, softcap=cap)
+                       for a, b in zip(cuts[:-1], cuts[1:])])
+        comb = orc.combine_shards(st, labels, reduction, zloss_coef=0.02, v_total=V)
+        np.testing.assert_allclose(comb["lse"], whole["lse"], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(comb["ez"], whole["ez"], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(comb["loss"], whole["loss"], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(comb["entropy"], whole["entropy"], rtol=1e-12, atol=1e-12)
+        dh = np.zeros_like(dh_w)
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            dhp, dwp = orc.backward(hidden, weight[:, a:b], labels, comb["lse"], comb["ez"], gl,
+                                    ge, reduction, zloss_coef=0.02, softcap=cap, v_offset=a,
+                                    v_total=V)
+            dh += dhp
+            np.testing.assert_allclose(dwp, dw_w[:, a:b], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dh, dh_w, rtol=1e-11, atol=1e-13)

@@ -1,0 +1,71 @@
+"""The vocabulary-parallel exchange on two CPU ranks (gloo).
+
+Each rank holds half of the vocabulary, computes its shard's softmax statistics with
+the oracle, exchanges them with the package's exchange_stats (an all-gather), merges
+them, and sums its shard's dhidden term with reduce_dhidden (an all-reduce).  The
+results must equal the whole-vocabulary oracle: this covers the collective steps of
+the sharded path without a GPU.
+"""
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, reduction, cap):
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from linear_cross_entropy_forward_gb300.vocab_parallel import exchange_stats, reduce_dhidden
+    from oracle import flce_oracle as orc
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        rng = np.random.default_rng(7)
+        N, H, V = 19, 11, 83
+        hidden = rng.standard_normal((N, H))
+        weight = rng.standard_normal((H, V)) * 0.9
+        labels = rng.integers(0, V, N)
+        labels[[2, 9]] = orc.IGNORE_INDEX
+        g_loss = rng.standard_normal(N) if reduction == "none" else np.array([0.8])
+        g_ent = rng.standard_normal(N) if reduction == "none" else np.array([-0.6])
+        cuts = np.linspace(0, V, world + 1).astype(int)
+        a, b = int(cuts[rank]), int(cuts[rank + 1])
+        local = torch.from_numpy(orc.shard_stats(hidden, weight[:, a:b], labels, a, cap))
+        gathered = exchange_stats(local)
+        assert gathered.shape == (world, 4, N)
+        comb = orc.combine_shards(gathered.numpy(), labels, reduction, zloss_coef=0.01,
+                                  v_total=V)
+        whole = orc.forward(hidden, weight, labels, reduction, zloss_coef=0.01, softcap=cap)
+        np.testing.assert_allclose(comb["loss"], whole["loss"], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(comb["entropy"], whole["entropy"], rtol=1e-12, atol=1e-12)
+        dh_part, dw_part = orc.backward(hidden, weight[:, a:b], labels, comb["lse"], comb["ez"],
+                                        g_loss, g_ent, reduction, zloss_coef=0.01, softcap=cap,
+                                        v_offset=a, v_total=V)
+        dh = reduce_dhidden(torch.from_numpy(dh_part)).numpy()
+        dh_w, dw_w = orc.backward(hidden, weight, labels, whole["lse"], whole["ez"], g_loss,
+                                  g_ent, reduction, zloss_coef=0.01, softcap=cap)
+        np.testing.assert_allclose(dh, dh_w, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dw_part, dw_w[:, a:b], rtol=1e-11, atol=1e-13)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("reduction,cap", [("mean", 0.0), ("none", 2.0), ("sum", 0.0)])
+def test_two_rank_vocab_parallel_exchange(reduction, cap):
+    mp.spawn(_worker, args=(2, _free_port(), reduction, cap), nprocs=2, join=True)
+
+
+def test_three_rank_vocab_parallel_exchange():
+    mp.spawn(_worker, args=(3, _free_port(), "mean", 1.5), nprocs=3, join=True)
