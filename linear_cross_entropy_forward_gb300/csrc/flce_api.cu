@@ -418,6 +418,12 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// L2 sector promotion of operand loads (CUtensorMapL2promotion: 0 none, 1 64 B,
+// 2 128 B, 3 256 B).
+#ifndef FLCE_L2_PROMOTION
+#define FLCE_L2_PROMOTION 3
+#endif
+
 // 2-D bf16 tensor map over a row-major [outer, inner] array with a {box_inner, box_outer}
 // box, 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
@@ -430,7 +436,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             static_cast<CUtensorMapL2promotion>(FLCE_L2_PROMOTION),
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -486,6 +492,31 @@ int raster_group(int64_t panel_bytes, int fast_tiles) {
   int64_t g = FLCE_L2_PANEL_BUDGET / panel_bytes;
   if (g < 1) g = 1;
   return g < fast_tiles ? static_cast<int>(g) : fast_tiles;
+}
+
+// Two CTA pairs per cluster share one operand (halving its L2 requests): along a
+// dimension with an even tile count (no spare tile), else along the longer one; a
+// single tile keeps one pair per cluster.  `panel_bytes` is the revisited operand's
+// size per tile of the fast raster dimension; the group is counted in cluster tiles.
+#ifndef FLCE_CLUSTER_SHARE
+#define FLCE_CLUSTER_SHARE 1
+#endif
+void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
+  int share = 0;
+  if (FLCE_CLUSTER_SHARE && tn == 256) {
+    if (sh->m_tiles % 2 == 0)
+      share = 1;
+    else if (sh->n_tiles % 2 == 0)
+      share = 2;
+    else if (int64_t(sh->m_tiles) * sh->n_tiles > 1)
+      share = sh->m_tiles >= sh->n_tiles ? 1 : 2;
+  }
+  sh->share = share;
+  const bool m_fast = sh->raster == 0;
+  const int cm = share == 1 ? (sh->m_tiles + 1) / 2 : sh->m_tiles;
+  const int cn = share == 2 ? (sh->n_tiles + 1) / 2 : sh->n_tiles;
+  const bool fast_shared = m_fast ? share == 1 : share == 2;
+  sh->group = raster_group(panel_bytes * (fast_shared ? 2 : 1), m_fast ? cm : cn);
 }
 
 GemmShape base_shape(int a_hint, int b_hint) {
@@ -567,9 +598,9 @@ int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
   const int64_t N = p->N, H = p->H, V = p->V;
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, hidden, H, N, H, BK, 128)) return FLCE_ERR_CUDA;
-  // weight as B: [H,V] is MN-major ({64,64} boxes), [V,H] K-major ({64, TN/2} boxes)
-  if (!(vh ? make_map(&tmB, weight, H, V, H, BK, TN_FWD / 2)
+  if (!make_map(&tmA, hidden, H, N, H, BK, 64)) return FLCE_ERR_CUDA;
+  // weight as B: [H,V] is MN-major, [V,H] K-major ({64,64} boxes either way)
+  if (!(vh ? make_map(&tmB, weight, H, V, H, BK, 64)
            : make_map(&tmB, weight, V, H, V, 64, BK)))
     return FLCE_ERR_CUDA;
   // hidden is revisited by every vocabulary tile of its group; the weight streams
@@ -578,7 +609,7 @@ int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
   sh.n_tiles = static_cast<int>(cdiv(V, TN_FWD));
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
   sh.raster = 0;
-  sh.group = raster_group(int64_t(PAIR_BM) * H * 2, sh.m_tiles);
+  plan_tiles(&sh, int64_t(PAIR_BM) * H * 2, TN_FWD);
   EpiArgs ea{};
   ea.rows = static_cast<int>(N);
   ea.cols = static_cast<int>(V);
@@ -783,16 +814,16 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   // recompute's B and as dhidden's B, each K- or MN-major depending on its layout.
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   CUtensorMap mHidK, mHidMn, mDlMn, mDlK, mWRec, mWDh;
-  bool ok = make_map(&mHidK, hidden, H, N, H, BK, 128) &&
+  bool ok = make_map(&mHidK, hidden, H, N, H, BK, 64) &&
             make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
             make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
-            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, 128);
+            make_map(&mDlK, dl, L.Vc, N, L.Vc, BK, 64);
   if (vh)
-    ok = ok && make_map(&mWRec, weight, H, V, H, BK, TN_DLOGITS / 2) &&
+    ok = ok && make_map(&mWRec, weight, H, V, H, BK, 64) &&
          make_map(&mWDh, weight, H, V, H, 64, BK);
   else
     ok = ok && make_map(&mWRec, weight, V, H, V, 64, BK) &&
-         make_map(&mWDh, weight, V, H, V, BK, TN_DHIDDEN / 2);
+         make_map(&mWDh, weight, V, H, V, BK, 64);
   if (!ok) return FLCE_ERR_CUDA;
 
   for (int64_t c = 0; c < L.chunks; ++c) {
@@ -805,7 +836,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s3.n_tiles = static_cast<int>(cdiv(w, TN_DLOGITS));
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
     s3.raster = 0;
-    s3.group = raster_group(int64_t(PAIR_BM) * H * 2, s3.m_tiles);
+    plan_tiles(&s3, int64_t(PAIR_BM) * H * 2, TN_DLOGITS);
     s3.b_mn_off = static_cast<int>(v0);
     EpiArgs e3{};
     e3.rows = static_cast<int>(N);
@@ -840,7 +871,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       s4.m_tiles = static_cast<int>(cdiv(w, PAIR_BM));
       s4.n_tiles = static_cast<int>(cdiv(H, TN_DWEIGHT));
       s4.raster = 1;
-      s4.group = raster_group(int64_t(TN_DWEIGHT) * N * 2, s4.n_tiles);
+      plan_tiles(&s4, int64_t(TN_DWEIGHT) * N * 2, TN_DWEIGHT);
       e4.rows = static_cast<int>(w);
       e4.cols = static_cast<int>(H);
       e4.out = static_cast<__nv_bfloat16*>(dweight) + v0 * H;
@@ -849,7 +880,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
       s4.n_tiles = static_cast<int>(cdiv(w, TN_DWEIGHT));
       s4.raster = 0;
-      s4.group = raster_group(int64_t(PAIR_BM) * N * 2, s4.m_tiles);
+      plan_tiles(&s4, int64_t(PAIR_BM) * N * 2, TN_DWEIGHT);
       e4.rows = static_cast<int>(H);
       e4.cols = static_cast<int>(w);
       e4.col_base = static_cast<int>(v0);
@@ -867,7 +898,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));
     s5.raster = 1;
-    s5.group = raster_group(int64_t(TN_DHIDDEN) * w * 2, s5.n_tiles);
+    plan_tiles(&s5, int64_t(TN_DHIDDEN) * w * 2, TN_DHIDDEN);
     s5.b_k_off = static_cast<int>(v0);
     EpiArgs e5{};
     e5.rows = static_cast<int>(N);
