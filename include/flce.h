@@ -105,11 +105,14 @@ typedef struct {
    * Sharding excludes label_smoothing and class_weight. */
   int64_t v_offset;
   int64_t v_total;
+  /* flce_forward_backward's token chunk (a multiple of 512), 0 = auto: the largest
+   * chunk whose fp32 logits and bf16 dlogits fit in 8 GiB. */
+  int64_t chunk_n;
 } flce_params;
 
 /* Bytes of device workspace that flce_forward / flce_shard_stats (phase 0),
- * flce_backward (phase 1) or flce_combine_shards (phase 2) needs for these
- * parameters; 0 when the parameters are invalid.  The workspace is scratch: its
+ * flce_backward (phase 1), flce_combine_shards (phase 2) or flce_forward_backward
+ * (phase 3) needs for these parameters; 0 when the parameters are invalid.  The workspace is scratch: its
  * contents need not be preserved between calls. */
 size_t flce_workspace_size(const flce_params* params, int phase);
 
@@ -134,6 +137,32 @@ int flce_backward(const flce_params* params, const void* hidden, const void* wei
                   const int64_t* labels, const float* lse, const float* ez,
                   const float* g_loss, const float* g_entropy, void* dhidden, void* dweight,
                   void* workspace, size_t ws_bytes, void* stream);
+
+/* Forward and backward in one call, for callers that know the upstream gradients
+ * when they run the forward (Liger-Kernel PR #551, "gradient in forward"; in a
+ * training step the loss's gradient is 1, scaled by the reduction).  Per chunk of
+ * params->chunk_n tokens the logits are computed once, kept in the workspace in
+ * fp32 next to their online-softmax statistics, turned into dlogits once the
+ * rows' logsumexp is known, and contracted into dhidden and dweight: 6*N*H*V
+ * flops instead of flce_forward + flce_backward's 8*N*H*V (no recompute), at the
+ * cost of an [chunk_n, V] fp32 + bf16 workspace.
+ *   Arguments: as flce_forward's and flce_backward's (g_loss, g_entropy: [N] for
+ *   FLCE_RED_NONE, [1] otherwise, NULL = zero).  loss, entropy, lse, ez,
+ *   dhidden and dweight are all written, with the values the two-call path
+ *   gives (the dlogits are bitwise the same).  Vocabulary sharding
+ *   (v_total > 0 with a partial shard) is rejected with FLCE_ERR_BAD_ARG.
+ *   workspace: >= flce_workspace_size(params, 3) bytes, 256-byte aligned. */
+int flce_forward_backward(const flce_params* params, const void* hidden, const void* weight,
+                          const int64_t* labels, const float* g_loss, const float* g_entropy,
+                          float* loss, float* entropy, float* lse, float* ez, void* dhidden,
+                          void* dweight, void* workspace, size_t ws_bytes, void* stream);
+
+/* x[i] = bf16(g[0] * x[i]) for the n bf16 values at x (16-byte aligned), on
+ * `stream`; the kernel returns at once when g[0] == 1.  It scales
+ * flce_forward_backward's dhidden and dweight when the upstream gradient of the
+ * loss becomes known only after the forward (autograd's backward).  Not part of
+ * the pages' method: a helper of the gradient-in-forward mode. */
+int flce_scale_bf16(void* x, int64_t n, const float* g, void* stream);
 
 /* Vocabulary-parallel forward, step 1 (the softmax statistics are split over
  * shards of the vocabulary and merged with the online-softmax max-rescale).
@@ -164,8 +193,8 @@ int flce_combine_shards(const flce_params* params, const float* stats, int32_t n
 int flce_status(const void* workspace, void* stream);
 
 /* Number of kernels one call with these parameters enqueues (memsets not counted):
- * phase 0 flce_forward, 1 flce_backward, 2 flce_combine_shards, 3 flce_shard_stats;
- * -1 when invalid. */
+ * phase 0 flce_forward, 1 flce_backward, 2 flce_combine_shards, 3 flce_shard_stats,
+ * 4 flce_forward_backward; -1 when invalid. */
 int flce_kernel_launches(const flce_params* params, int phase);
 
 /* Static, NUL-terminated description of a status code. */

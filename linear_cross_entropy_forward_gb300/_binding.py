@@ -36,7 +36,7 @@ class FlceParams(ctypes.Structure):
                 ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64),
                 ("weight_layout", ctypes.c_int32), ("label_smoothing", ctypes.c_float),
                 ("class_weight", ctypes.c_void_p), ("v_offset", ctypes.c_int64),
-                ("v_total", ctypes.c_int64)]
+                ("v_total", ctypes.c_int64), ("chunk_n", ctypes.c_int64)]
 
 
 WEIGHT_HV, WEIGHT_VH = 0, 1
@@ -56,7 +56,8 @@ _lock = threading.Lock()
 
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
             "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc",
-            "flce_shard_stats", "flce_combine_shards")
+            "flce_shard_stats", "flce_combine_shards", "flce_forward_backward",
+            "flce_scale_bf16")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -89,6 +90,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flce_combine_shards.restype = ctypes.c_int
         lib.flce_kernel_launches.argtypes = [P, ctypes.c_int]
         lib.flce_kernel_launches.restype = ctypes.c_int
+        lib.flce_forward_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              ctypes.c_size_t, vp]
+        lib.flce_forward_backward.restype = ctypes.c_int
+        lib.flce_scale_bf16.argtypes = [vp, ctypes.c_int64, vp, vp]
+        lib.flce_scale_bf16.restype = ctypes.c_int
         lib.flce_version.argtypes = []
         lib.flce_version.restype = ctypes.c_int
         _lib = lib
@@ -102,15 +108,17 @@ def _check(code: int):
 
 def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
                 softcap=0.0, validate=False, chunk_v=0, weight_layout="hv",
-                label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0) -> FlceParams:
+                label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0,
+                chunk_n=0) -> FlceParams:
     """class_weight: a CUDA fp32 [V] tensor (kept alive by the caller) or None.
     v_offset / v_total: this weight is columns [v_offset, v_offset + V) of a vocabulary
-    of v_total entries (0: the whole vocabulary)."""
+    of v_total entries (0: the whole vocabulary).  chunk_n: token chunk of
+    flce_forward_backward (multiple of 512, 0 = auto)."""
     cw = class_weight.data_ptr() if class_weight is not None else None
     return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
                       float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v),
                       layout_code(weight_layout), float(label_smoothing), cw, int(v_offset),
-                      int(v_total))
+                      int(v_total), int(chunk_n))
 
 
 def _dims(hidden, weight, weight_layout):
@@ -235,6 +243,60 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     return dh, dw
 
 
+def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
+                          ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0,
+                          validate=False, chunk_n=0, workspace=None, stream=None, out=None,
+                          weight_layout="hv", label_smoothing=0.0, class_weight=None):
+    """Forward and backward in one call (the upstream gradients known up front).
+
+    g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
+    Returns (loss, entropy, lse, ez, dhidden, dweight) -- what flce_forward followed by
+    flce_backward returns -- at 6*N*H*V flops instead of 8*N*H*V.
+    """
+    lib = load_library()
+    N, H, V, wshape = _dims(hidden, weight, weight_layout)
+    _need(hidden, "hidden", torch.bfloat16, (N, H))
+    _need(weight, "weight", torch.bfloat16, wshape)
+    _need(labels, "labels", torch.int64, (N,))
+    if class_weight is not None:
+        _need(class_weight, "class_weight", torch.float32, (V,))
+    p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
+                    weight_layout=weight_layout, label_smoothing=label_smoothing,
+                    class_weight=class_weight, chunk_n=chunk_n)
+    n_g = N if p.reduction == RED_NONE else 1
+    if g_loss is not None:
+        _need(g_loss, "g_loss", torch.float32, (n_g,))
+    if g_entropy is not None:
+        _need(g_entropy, "g_entropy", torch.float32, (n_g,))
+    dev = hidden.device
+    if out is None:
+        loss = torch.empty(n_g, dtype=torch.float32, device=dev)
+        ent = torch.empty(n_g, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        ez = torch.empty(N, dtype=torch.float32, device=dev)
+        dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
+    else:
+        loss, ent, lse, ez, dh, dw = out
+    ws = _workspace(p, 3, dev, workspace)
+    _check(lib.flce_forward_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
+                                     _ptr(g_loss), _ptr(g_entropy), _ptr(loss), _ptr(ent),
+                                     _ptr(lse), _ptr(ez), _ptr(dh), _ptr(dw), _ptr(ws),
+                                     ws.numel(), _stream(stream)))
+    return loss, ent, lse, ez, dh, dw
+
+
+def flce_scale_bf16(x, g, stream=None):
+    """x *= g[0] in place (x: contiguous CUDA bf16, g: CUDA fp32 [1]); a no-op on the
+    device when g is exactly 1."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.bfloat16 \
+            or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA bf16 tensor")
+    _need(g, "g", torch.float32, (1,))
+    _check(load_library().flce_scale_bf16(_ptr(x), x.numel(), _ptr(g), _stream(stream)))
+    return x
+
+
 def flce_shard_stats(hidden, weight, labels, v_offset, v_total, softcap=0.0,
                      ignore_index=IGNORE_INDEX, weight_layout="hv", validate=False,
                      workspace=None, stream=None, out=None):
@@ -317,9 +379,41 @@ class _LinearCrossEntropy(torch.autograd.Function):
         return dh, dw, None, None, None, None, None, None, None, None
 
 
+class _LinearCrossEntropyGradInForward(torch.autograd.Function):
+    """The gradients of loss + entropy_coef * entropy are computed in the forward
+    (flce_forward_backward with g_loss = 1) and scaled by the loss's upstream
+    gradient in the backward; the entropy output carries no gradient of its own."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap,
+                weight_layout, label_smoothing, class_weight, entropy_coef):
+        if reduction_code(reduction) == RED_NONE:
+            raise ValueError("grad_in_forward needs reduction 'mean' or 'sum'")
+        dev = hidden.device
+        one = torch.ones(1, dtype=torch.float32, device=dev)
+        ce = torch.full((1,), float(entropy_coef), dtype=torch.float32, device=dev)
+        loss, ent, _, _, dh, dw = flce_forward_backward(
+            hidden, weight, labels, one, ce, reduction, ignore_index, zloss_coef, softcap,
+            weight_layout=weight_layout, label_smoothing=label_smoothing,
+            class_weight=class_weight)
+        ctx.save_for_backward(dh, dw)
+        ctx.mark_non_differentiable(ent)
+        return loss[0], ent[0]
+
+    @staticmethod
+    def backward(ctx, g_loss, g_ent):
+        dh, dw = ctx.saved_tensors
+        if g_loss is None:
+            return (None,) * 11
+        g = g_loss.detach().reshape(1).to(torch.float32).contiguous()
+        flce_scale_bf16(dh, g)
+        flce_scale_bf16(dw, g)
+        return dh, dw, None, None, None, None, None, None, None, None, None
+
+
 def linear_cross_entropy(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
                          zloss_coef=0.0, softcap=0.0, weight_layout="hv", label_smoothing=0.0,
-                         class_weight=None):
+                         class_weight=None, grad_in_forward=False, entropy_coef=0.0):
     """loss, entropy = linear_cross_entropy(hidden, weight, labels, reduction)
 
     The call of verl PR #462 ("API"): hidden [N,H] bf16, weight [H,V] bf16,
@@ -328,7 +422,17 @@ def linear_cross_entropy(hidden, weight, labels, reduction="mean", ignore_index=
     and weight.  weight_layout='vh' takes an nn.Linear-style weight [V,H];
     label_smoothing and class_weight (fp32 [V], not differentiated) follow torch's
     cross_entropy.
+
+    grad_in_forward=True (reduction 'mean' or 'sum'; Liger-Kernel PR #551's
+    gradient in forward): the forward also computes the gradients of
+    loss + entropy_coef * entropy, with no recompute in the backward, which only
+    scales them by the loss's upstream gradient.  The entropy output is then not
+    differentiable: its weight in the objective is entropy_coef.
     """
+    if grad_in_forward:
+        return _LinearCrossEntropyGradInForward.apply(
+            hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap, weight_layout,
+            label_smoothing, class_weight, entropy_coef)
     return _LinearCrossEntropy.apply(hidden, weight, labels, reduction, ignore_index,
                                      zloss_coef, softcap, weight_layout, label_smoothing,
                                      class_weight)

@@ -12,6 +12,11 @@
 //   5. bwd_dweight GEMM: dweight[:, chunk] = hidden^T @ dlogits.
 //   6. bwd_dhidden GEMM: dhidden (fp32 accumulator) += dlogits @ weight[:, chunk]^T;
 //      the last chunk writes bf16.
+// Forward + backward in one call (gradient in forward), per chunk of tokens:
+//   1. fwd_stats GEMM that also keeps the raw fp32 logits of the chunk,
+//   2. combine, prep, then dlogits from the kept logits (no recompute),
+//   3. dhidden rows of the chunk = dlogits @ weight^T (all of V in one GEMM),
+//   4. dweight = hidden^T @ dlogits, written once (one chunk) or accumulated.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -26,7 +31,7 @@ namespace flce {
 
 namespace {
 
-constexpr int kVersion = 100;  // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0
 constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr int64_t kDefaultChunkBytes = int64_t(256) << 20;  // dlogits chunk target
@@ -250,18 +255,20 @@ __global__ void __launch_bounds__(256) shard_stats_kernel(
 //   A1 = a_ce ((1 - eps) w_y + eps W / V) + 2 coef lse a_z + b Ez,
 //   C_y = a_ce (1 - eps) w_y,  D = a_ce eps / V,
 // so that dlogits = p (A1 - b z) - C_y [v == y] - D w_v.
+// The mean's denominators count the rows of den_labels [den_n] (all rows of the
+// call), the constants are written for the N rows of labels (a chunk of them).
 __global__ void __launch_bounds__(1024) bwd_prep_kernel(
-    const int64_t* __restrict__ labels, const float* __restrict__ lse,
-    const float* __restrict__ ez, const float* __restrict__ g_loss,
-    const float* __restrict__ g_ent, int64_t N, int64_t V, int64_t ignore_index, int per_token,
-    int mean, float zcoef, float eps, const float* __restrict__ cw, float4* __restrict__ rowc,
-    float* __restrict__ rowd) {
+    const int64_t* __restrict__ labels, const int64_t* __restrict__ den_labels, int64_t den_n,
+    const float* __restrict__ lse, const float* __restrict__ ez,
+    const float* __restrict__ g_loss, const float* __restrict__ g_ent, int64_t N, int64_t V,
+    int64_t ignore_index, int per_token, int mean, float zcoef, float eps,
+    const float* __restrict__ cw, float4* __restrict__ rowc, float* __restrict__ rowd) {
   __shared__ long long sc[1024];
   __shared__ double sw[1024], sww[1024];
   long long c = 0;
   double wy_sum = 0.0, w_all = 0.0;
-  for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
-    const int64_t y = labels[n];
+  for (int64_t n = threadIdx.x; n < den_n; n += blockDim.x) {
+    const int64_t y = den_labels[n];
     if (y != ignore_index) {
       ++c;
       if (cw) wy_sum += cw[y];
@@ -307,6 +314,68 @@ __global__ void __launch_bounds__(1024) bwd_prep_kernel(
                      fmaf(2.0f * zcoef * l, a, b * ez[n]);
     rowc[n] = make_float4(l * kLog2e, a1, b, cy);
     if (eps != 0.0f) rowd[n] = a_ce * eps / static_cast<float>(V);
+  }
+}
+
+// dlogits [rows, ldz] (bf16) from the raw fp32 logits z [rows, ldz] the forward
+// GEMM kept, with the per-row constants of bwd_prep_kernel; the same per-element
+// arithmetic as the recompute epilogue (dlogit_of), zero beyond column V.
+__global__ void __launch_bounds__(256) dlogits_from_z_kernel(
+    const float* __restrict__ z, int64_t rows, int64_t ldz, const float4* __restrict__ rowc,
+    const float* __restrict__ rowd, const int64_t* __restrict__ labels, int64_t V,
+    float softcap, int smooth, const float* __restrict__ cw, __nv_bfloat16* __restrict__ dl) {
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (c0 >= ldz) return;
+  const bool cap = softcap != 0.0f;
+  const float inv_cap = cap ? 1.0f / softcap : 0.0f;
+  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const float4 rc = rowc[row];
+    const float dcoef = smooth ? rowd[row] : 0.0f;
+    const int64_t yl = labels[row];
+    const int64_t y = (yl >= 0 && yl < V) ? yl : -1;
+    const float4 za = *reinterpret_cast<const float4*>(z + row * ldz + c0);
+    const float4 zb = *reinterpret_cast<const float4*>(z + row * ldz + c0 + 4);
+    const float x[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+    uint32_t pk[4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      float g2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t v = c0 + j + h;
+        const bool in = v < V;
+        const float dw = (smooth && in) ? __fmul_rn(dcoef, cw ? __ldg(cw + v) : 1.0f) : 0.0f;
+        const float g = dlogit_of(x[j + h], rc, v == y, smooth != 0, dw, cap, softcap, inv_cap);
+        g2[h] = in ? g : 0.0f;
+      }
+      pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+    }
+    *reinterpret_cast<uint4*>(dl + row * ldz + c0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// x *= g[0] over n bf16 values, 8 per thread (grid-stride); nothing when g[0] == 1.
+__global__ void __launch_bounds__(256) scale_bf16_kernel(__nv_bfloat16* __restrict__ x,
+                                                         int64_t n, const float* __restrict__ g) {
+  const float s = *g;
+  if (s == 1.0f) return;
+  const int64_t n8 = n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    uint4 v = reinterpret_cast<uint4*>(x)[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16);
+      const float hi = __uint_as_float(w[k] & 0xffff0000u);
+      w[k] = pack_bf16x2(lo * s, hi * s);
+    }
+    reinterpret_cast<uint4*>(x)[i] = v;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n - n8 * 8) {
+    const int64_t i = n8 * 8 + threadIdx.x;
+    x[i] = __float2bfloat16_rn(__bfloat162float(x[i]) * s);
   }
 }
 
@@ -372,6 +441,51 @@ BwdLayout bwd_layout(const flce_params* p) {
   return L;
 }
 
+// Token chunk of flce_forward_backward: the rows whose fp32 logits and bf16
+// dlogits fit FLCE_FUSED_BUDGET, a multiple of 512 rows (two pair tiles), capped
+// at N rounded up to a whole 256-row tile.
+#ifndef FLCE_FUSED_BUDGET
+#define FLCE_FUSED_BUDGET (int64_t(8) << 30)
+#endif
+
+struct FusedLayout {
+  size_t pm, pd, ps, psw, zlabel, loss_row, ent_row, rowc, rowd, z, dl, dwacc, total;
+  int64_t Nc, chunks, ldz, n_parts;
+};
+
+FusedLayout fused_layout(const flce_params* p) {
+  FusedLayout L{};
+  L.ldz = cdiv(p->V, 256) * 256;
+  int64_t nc = p->chunk_n;
+  if (nc <= 0) nc = FLCE_FUSED_BUDGET / (L.ldz * 6) / 512 * 512;
+  if (nc < 512) nc = 512;
+  const int64_t ncap = cdiv(p->N > 0 ? p->N : 1, 256) * 256;
+  L.Nc = nc < ncap ? nc : ncap;
+  L.chunks = cdiv(p->N, L.Nc);
+  L.n_parts = 2 * cdiv(p->V, TN_FWD);
+  const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * L.Nc) * 4);
+  const size_t chunk_row_bytes = align256(static_cast<size_t>(L.Nc) * 4);
+  const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
+  size_t off = kHeaderBytes;
+  L.pm = off; off += part_bytes;
+  L.pd = off; off += part_bytes;
+  L.ps = off; off += part_bytes;
+  L.psw = off;
+  if (p->label_smoothing != 0.0f) off += part_bytes;
+  L.zlabel = off; off += chunk_row_bytes;
+  L.loss_row = off; off += row_bytes;
+  L.ent_row = off; off += row_bytes;
+  L.rowc = off; off += align256(static_cast<size_t>(L.Nc) * 16);
+  L.rowd = off;
+  if (p->label_smoothing != 0.0f) off += chunk_row_bytes;
+  L.z = off; off += align256(static_cast<size_t>(L.Nc * L.ldz) * 4);
+  L.dl = off; off += align256(static_cast<size_t>(L.Nc * L.ldz) * 2);
+  L.dwacc = off;
+  if (L.chunks > 1) off += align256(static_cast<size_t>(p->H * p->V) * 4);
+  L.total = off;
+  return L;
+}
+
 int check_params(const flce_params* p) {
   if (!p) return FLCE_ERR_BAD_ARG;
   if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_SUM) return FLCE_ERR_BAD_ARG;
@@ -380,6 +494,7 @@ int check_params(const flce_params* p) {
   if (p->N > kMaxDim || p->H > kMaxDim || p->V > kMaxDim) return FLCE_ERR_BAD_SHAPE;
   if (p->H % 8 != 0 || p->V % 8 != 0) return FLCE_ERR_ALIGN;
   if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % 256 != 0)) return FLCE_ERR_BAD_ARG;
+  if (p->chunk_n < 0 || p->chunk_n % 512 != 0) return FLCE_ERR_BAD_ARG;
   if (p->weight_layout != FLCE_WEIGHT_HV && p->weight_layout != FLCE_WEIGHT_VH)
     return FLCE_ERR_BAD_ARG;
   if (!(p->label_smoothing >= 0.0f && p->label_smoothing <= 1.0f)) return FLCE_ERR_BAD_ARG;
@@ -560,6 +675,7 @@ size_t flce_workspace_size(const flce_params* p, int phase) {
   if (phase == 0) return fwd_layout(p).total;
   if (phase == 1) return bwd_layout(p).total;
   if (phase == 2) return kHeaderBytes + 2 * align256(static_cast<size_t>(p->N) * 4);
+  if (phase == 3) return fused_layout(p).total;
   return 0;
 }
 
@@ -575,6 +691,9 @@ int flce_kernel_launches(const flce_params* p, int phase) {
       return 1 + reduce;
     case 3:  // flce_shard_stats: GEMM, shard merge
       return 2;
+    case 4:  // flce_forward_backward: [class-weight sum], 6 per token chunk, [reduce]
+      return 6 * static_cast<int>(fused_layout(p).chunks) + reduce +
+             (p->label_smoothing != 0.0f && p->class_weight ? 1 : 0);
     default:
       return -1;
   }
@@ -590,11 +709,19 @@ int flce_status(const void* workspace, void* stream) {
 namespace flce {
 namespace {
 
-// Stage 1 of the forward: logits tiles of hidden @ weight reduced to per-row,
-// per-column-block online-softmax partials (and the label logit) in the workspace.
-int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
-                  const int64_t* labels, uint8_t* ws, const FwdLayout& L, uint32_t* err,
-                  cudaStream_t st, EpiArgs* ea_out) {
+// Where the forward GEMM's epilogue writes: per-row, per-column-block partials
+// (part p of row n at p * part_stride + n), the label logits, and optionally the
+// raw fp32 logits [rows, ld_z].
+struct StatsOut {
+  float *pm, *pd, *ps, *psw, *zlabel, *zout;
+  int64_t part_stride, ld_z;
+};
+
+// Logits tiles of hidden rows [n0, n0 + rows) @ weight reduced to online-softmax
+// partials; `labels` points at row n0's label.
+int launch_stats(const flce_params* p, const void* hidden, const void* weight,
+                 const int64_t* labels, int64_t n0, int64_t rows, const StatsOut& o,
+                 uint32_t* err, cudaStream_t st) {
   const int64_t N = p->N, H = p->H, V = p->V;
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   CUtensorMap tmA, tmB;
@@ -605,13 +732,14 @@ int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
     return FLCE_ERR_CUDA;
   // hidden is revisited by every vocabulary tile of its group; the weight streams
   GemmShape sh = base_shape(L2_EVICT_LAST, L2_NORMAL);
-  sh.m_tiles = static_cast<int>(cdiv(N, PAIR_BM));
+  sh.m_tiles = static_cast<int>(cdiv(rows, PAIR_BM));
   sh.n_tiles = static_cast<int>(cdiv(V, TN_FWD));
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
+  sh.a_mn_off = static_cast<int>(n0);
   sh.raster = 0;
   plan_tiles(&sh, int64_t(PAIR_BM) * H * 2, TN_FWD);
   EpiArgs ea{};
-  ea.rows = static_cast<int>(N);
+  ea.rows = static_cast<int>(rows);
   ea.cols = static_cast<int>(V);
   ea.col_base = 0;
   ea.V = V;
@@ -619,17 +747,33 @@ int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
   ea.labels = labels;
   ea.label_offset = p->v_offset;
   ea.ignore_index = p->ignore_index;
-  ea.pm = reinterpret_cast<float*>(ws + L.pm);
-  ea.pd = reinterpret_cast<float*>(ws + L.pd);
-  ea.ps = reinterpret_cast<float*>(ws + L.ps);
-  ea.part_stride = N;
-  ea.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
+  ea.pm = o.pm;
+  ea.pd = o.pd;
+  ea.ps = o.ps;
+  ea.part_stride = o.part_stride;
+  ea.zlabel = o.zlabel;
   ea.smooth = p->label_smoothing;
   ea.cw = p->class_weight;
-  ea.psw = reinterpret_cast<float*>(ws + L.psw);
+  ea.psw = o.psw;
+  ea.zout = o.zout;
+  ea.ld_z = o.ld_z;
   ea.err = err;
-  *ea_out = ea;
   return cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st));
+}
+
+// Stage 1 of the forward over all rows, into the forward workspace layout.
+int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
+                  const int64_t* labels, uint8_t* ws, const FwdLayout& L, uint32_t* err,
+                  cudaStream_t st, StatsOut* out) {
+  StatsOut o{};
+  o.pm = reinterpret_cast<float*>(ws + L.pm);
+  o.pd = reinterpret_cast<float*>(ws + L.pd);
+  o.ps = reinterpret_cast<float*>(ws + L.ps);
+  o.psw = reinterpret_cast<float*>(ws + L.psw);
+  o.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
+  o.part_stride = p->N;
+  *out = o;
+  return launch_stats(p, hidden, weight, labels, 0, p->N, o, err, st);
 }
 
 // Stage 2: per-row outputs from the merged parts, then the reduction over rows.
@@ -699,7 +843,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
     if ((rc = zero_reduced(p, loss, entropy, st))) return rc;
     return p->validate ? read_status(ws, st) : FLCE_OK;
   }
-  EpiArgs ea;
+  StatsOut ea;
   if ((rc = run_fwd_stats(p, hidden, weight, labels, ws, L, err, st, &ea))) return rc;
   Smoothing sm{p->label_smoothing, p->class_weight, ea.psw, nullptr};
   if (p->label_smoothing != 0.0f && p->class_weight) {
@@ -731,7 +875,7 @@ int flce_shard_stats(const flce_params* p, const void* hidden, const void* weigh
   if ((rc = begin_call(workspace, ws_bytes, L.total, stream, &st, &err))) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (p->N > 0) {
-    EpiArgs ea;
+    StatsOut ea;
     if ((rc = run_fwd_stats(p, hidden, weight, labels, ws, L, err, st, &ea))) return rc;
     shard_stats_kernel<<<static_cast<unsigned>(cdiv(p->N, 32)), 256, 0, st>>>(
         ea.pm, ea.pd, ea.ps, L.n_parts, p->N, ea.zlabel, labels, p->v_offset, p->V, stats);
@@ -803,7 +947,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + L.dl);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
   float* rowd = reinterpret_cast<float*>(ws + L.rowd);
-  bwd_prep_kernel<<<1, 1024, 0, st>>>(labels, lse, ez, g_loss, g_entropy, N, V, p->ignore_index,
+  bwd_prep_kernel<<<1, 1024, 0, st>>>(labels, labels, N, lse, ez, g_loss, g_entropy, N, V,
+                                      p->ignore_index,
                                       p->reduction == FLCE_RED_NONE,
                                       p->reduction == FLCE_RED_MEAN, p->zloss_coef,
                                       p->label_smoothing, p->class_weight, rowc, rowd);
@@ -917,6 +1062,189 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       return rc;
   }
   return p->validate ? read_status(ws, st) : FLCE_OK;
+}
+
+int flce_forward_backward(const flce_params* p, const void* hidden, const void* weight,
+                          const int64_t* labels, const float* g_loss, const float* g_entropy,
+                          float* loss, float* entropy, float* lse, float* ez, void* dhidden,
+                          void* dweight, void* workspace, size_t ws_bytes, void* stream) {
+  using namespace flce;
+  int rc = check_params(p);
+  if (rc) return rc;
+  // the dlogits of a shard need the whole vocabulary's logsumexp first
+  if (p->v_total > 0 && !(p->v_offset == 0 && p->v_total == p->V)) return FLCE_ERR_BAD_ARG;
+  if (!loss || !entropy || !workspace || !weight || !dweight) return FLCE_ERR_BAD_ARG;
+  if (p->N > 0 && (!hidden || !labels || !lse || !ez || !dhidden)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(loss) ||
+      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) || !aligned16(dhidden) ||
+      !aligned16(dweight) || (reinterpret_cast<uintptr_t>(g_loss) & 3) ||
+      (reinterpret_cast<uintptr_t>(g_entropy) & 3) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FLCE_ERR_ALIGN;
+  const FusedLayout L = fused_layout(p);
+  cudaStream_t st;
+  uint32_t* err;
+  if ((rc = begin_call(workspace, ws_bytes, L.total, stream, &st, &err))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t N = p->N, H = p->H, V = p->V;
+  if (N == 0) {
+    if ((rc = zero_reduced(p, loss, entropy, st))) return rc;
+    if ((rc = cuda_rc(cudaMemsetAsync(dweight, 0, static_cast<size_t>(H * V) * 2, st))))
+      return rc;
+    return p->validate ? read_status(ws, st) : FLCE_OK;
+  }
+  const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
+  const bool per_token = p->reduction == FLCE_RED_NONE;
+  const bool smooth = p->label_smoothing != 0.0f;
+  Smoothing sm{p->label_smoothing, p->class_weight, reinterpret_cast<float*>(ws + L.psw),
+               nullptr};
+  if (smooth && p->class_weight) {
+    float* wsum = reinterpret_cast<float*>(ws + kWsumOffset);
+    class_weight_sum_kernel<<<1, 1024, 0, st>>>(p->class_weight, V, wsum);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+    sm.wsum = wsum;
+  }
+  StatsOut so{};
+  so.pm = reinterpret_cast<float*>(ws + L.pm);
+  so.pd = reinterpret_cast<float*>(ws + L.pd);
+  so.ps = reinterpret_cast<float*>(ws + L.ps);
+  so.psw = reinterpret_cast<float*>(ws + L.psw);
+  so.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
+  so.zout = reinterpret_cast<float*>(ws + L.z);
+  so.part_stride = L.Nc;
+  so.ld_z = L.ldz;
+  float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
+  float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
+  float4* rowc = reinterpret_cast<float4*>(ws + L.rowc);
+  float* rowd = reinterpret_cast<float*>(ws + L.rowd);
+  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + L.dl);
+  float* dwacc = reinterpret_cast<float*>(ws + L.dwacc);
+
+  // hidden as dweight's operand (MN-major, tokens along K); weight as dhidden's B
+  CUtensorMap mHidMn, mWDh;
+  bool ok = make_map(&mHidMn, hidden, H, N, H, 64, BK);
+  ok = ok && (vh ? make_map(&mWDh, weight, H, V, H, 64, BK)
+                 : make_map(&mWDh, weight, V, H, V, BK, 64));
+  if (!ok) return FLCE_ERR_CUDA;
+
+  for (int64_t c = 0; c < L.chunks; ++c) {
+    const int64_t n0 = c * L.Nc;
+    const int64_t rows = (N - n0) < L.Nc ? (N - n0) : L.Nc;
+    const int64_t* lab = labels + n0;
+
+    // logits of the chunk: online-softmax partials and the raw fp32 values
+    if ((rc = launch_stats(p, hidden, weight, lab, n0, rows, so, err, st))) return rc;
+    const Parts pt{so.pm, so.pd, so.ps, nullptr, L.n_parts, L.Nc};
+    fwd_combine_kernel<<<static_cast<unsigned>(cdiv(rows, 32)), 256, 0, st>>>(
+        pt, rows, so.zlabel, lab, V, p->ignore_index, p->zloss_coef, sm, lse + n0, ez + n0,
+        loss_row + n0, ent_row + n0, err);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+    bwd_prep_kernel<<<1, 1024, 0, st>>>(
+        lab, labels, N, lse + n0, ez + n0, g_loss && per_token ? g_loss + n0 : g_loss,
+        g_entropy && per_token ? g_entropy + n0 : g_entropy, rows, V, p->ignore_index,
+        per_token, p->reduction == FLCE_RED_MEAN, p->zloss_coef, p->label_smoothing,
+        p->class_weight, rowc, rowd);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+    {
+      const dim3 grid(static_cast<unsigned>(cdiv(L.ldz / 8, 256)),
+                      static_cast<unsigned>(rows < 65535 ? rows : 65535));
+      dlogits_from_z_kernel<<<grid, 256, 0, st>>>(so.zout, rows, L.ldz, rowc, rowd, lab, V,
+                                                  p->softcap, smooth ? 1 : 0, p->class_weight,
+                                                  dl);
+      if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+    }
+
+    // the chunk's dlogits [rows, V]: rows past `rows` read as zeros
+    CUtensorMap mDlK, mDlMn;
+    ok = make_map(&mDlK, dl, V, rows, L.ldz, BK, 64) &&
+         make_map(&mDlMn, dl, V, rows, L.ldz, 64, BK);
+    if (!ok) return FLCE_ERR_CUDA;
+
+    // dhidden[n0 : n0 + rows] = dlogits @ weight^T, all of V in one contraction;
+    // the k-steps of every tile advance together, so a square-ish group of tiles
+    // keeps the k-slices in flight small in L2
+    GemmShape s5 = base_shape(L2_NORMAL, L2_NORMAL);
+    s5.m_tiles = static_cast<int>(cdiv(rows, PAIR_BM));
+    s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
+    s5.k_blocks = static_cast<int>(cdiv(V, BK));
+    s5.raster = 0;
+    plan_tiles(&s5, int64_t(PAIR_BM) * V * 2, TN_DHIDDEN);
+    s5.group = s5.share == 1 ? 4 : 8;
+    EpiArgs e5{};
+    e5.rows = static_cast<int>(rows);
+    e5.cols = static_cast<int>(H);
+    e5.V = V;
+    e5.acc_out = static_cast<__nv_bfloat16*>(dhidden) + n0 * H;
+    e5.ld_acc = H;
+    e5.acc_mode = ACC_ONLY;
+    e5.err = err;
+    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK, mWDh, s5, e5,
+                                                                        st))))
+      return rc;
+
+    // dweight (+)= hidden[n0 : n0 + rows]^T @ dlogits ([H,V]) or its transpose ([V,H])
+    GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
+    s4.k_blocks = static_cast<int>(cdiv(rows, BK));
+    EpiArgs e4{};
+    e4.V = V;
+    e4.err = err;
+    e4.col_base = 0;
+    if (vh) {
+      s4.m_tiles = static_cast<int>(cdiv(V, PAIR_BM));
+      s4.n_tiles = static_cast<int>(cdiv(H, TN_DWEIGHT));
+      s4.b_k_off = static_cast<int>(n0);
+      s4.raster = 1;
+      plan_tiles(&s4, int64_t(TN_DWEIGHT) * rows * 2, TN_DWEIGHT);
+      e4.rows = static_cast<int>(V);
+      e4.cols = static_cast<int>(H);
+    } else {
+      s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
+      s4.n_tiles = static_cast<int>(cdiv(V, TN_DWEIGHT));
+      s4.a_k_off = static_cast<int>(n0);
+      s4.raster = 0;
+      plan_tiles(&s4, int64_t(PAIR_BM) * rows * 2, TN_DWEIGHT);
+      e4.rows = static_cast<int>(H);
+      e4.cols = static_cast<int>(V);
+    }
+    const int64_t ld_dw = vh ? H : V;
+    const CUtensorMap& a4 = vh ? mDlMn : mHidMn;
+    const CUtensorMap& b4 = vh ? mHidMn : mDlMn;
+    if (L.chunks == 1) {
+      e4.out = static_cast<__nv_bfloat16*>(dweight);
+      e4.ld_out = ld_dw;
+      rc = cuda_rc(launch_bwd_dweight(a4, b4, s4, e4, st));
+    } else {
+      e4.acc = dwacc;
+      e4.acc_out = static_cast<__nv_bfloat16*>(dweight);
+      e4.ld_acc = ld_dw;
+      e4.acc_mode = c == 0 ? ACC_FIRST : c == L.chunks - 1 ? ACC_LAST : ACC_MID;
+      rc = cuda_rc(launch_bwd_dweight_acc(a4, b4, s4, e4, st));
+    }
+    if (rc) return rc;
+  }
+  if (!per_token) {
+    reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,
+                                           p->reduction == FLCE_RED_MEAN, p->class_weight, lse,
+                                           p->zloss_coef, loss, entropy);
+    if ((rc = cuda_rc(cudaGetLastError()))) return rc;
+  }
+  return p->validate ? read_status(ws, st) : FLCE_OK;
+}
+
+int flce_scale_bf16(void* x, int64_t n, const float* g, void* stream) {
+  using namespace flce;
+  if (n < 0 || !g || (n > 0 && !x)) return FLCE_ERR_BAD_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(g) & 3)) return FLCE_ERR_ALIGN;
+  if (n == 0) return FLCE_OK;
+  DevInfo di;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  const int64_t blocks = cdiv(cdiv(n, 8), 256);
+  const int64_t cap = int64_t(di.sms) * 8;
+  scale_bf16_kernel<<<static_cast<unsigned>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256,
+                      0, static_cast<cudaStream_t>(stream)>>>(static_cast<__nv_bfloat16*>(x), n,
+                                                              g);
+  return cuda_rc(cudaGetLastError());
 }
 
 }  // extern "C"

@@ -122,6 +122,8 @@ struct EpiArgs {
   float smooth;
   const float* cw;
   float* psw;           // FWD_STATS: per part sum_v w_v z_v (same layout as pm)
+  float* zout;          // FWD_STATS: if set, the raw fp32 accumulators, [rows, ld_z]
+  int64_t ld_z;
   // EPI_DLOGITS
   const float4* rowc;   // per row: (lse*log2e, A1, b, C_y), see bwd_prep_kernel
   const float* rowd;    // per row: D, the coefficient of -w_v (label smoothing)
@@ -237,12 +239,20 @@ struct Epilogue<EPI_FWD_STATS> {
     const bool smooth = ea.smooth != 0.0f;
     float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f, sw = 0.0f;
     bool hit = false;
+    float* zrow = (ea.zout && row_ok) ? ea.zout + static_cast<int64_t>(row) * ea.ld_z + col0
+                                      : nullptr;
 #pragma unroll 1
     for (int c = 0; c < CH; ++c) {
       float x[32];
       tmem_ld32(tbase + c * 32, x);
       const int vb = vcol0 + c * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
+      if (zrow) {
+        float4* z4 = reinterpret_cast<float4*>(zrow + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          z4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      }
       if (cap) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = ea.softcap * tanh_from_exp(x[j] * inv_cap);
@@ -300,6 +310,28 @@ struct Epilogue<EPI_FWD_STATS> {
   }
 };
 
+// dlogit of one logit from its raw fp32 accumulator x, with the row's constants
+// rc = (lse log2e, A1, b, C_y) and dw = D w_v (label smoothing, else 0):
+//   z = c tanh(x / c) (soft-cap, c != 0),  p = 2^{z log2e - lse log2e},
+//   g = p (A1 - b z) - C_y [v == y] - D w_v,  times 1 - tanh^2 under the cap.
+// Products that feed a sum are rounded explicitly, so every caller (the GEMM
+// epilogue, the gradient-in-forward kernel) gets the same bits.
+__device__ __forceinline__ float dlogit_of(float x, const float4& rc, bool is_label, bool smooth,
+                                           float dw, bool cap, float softcap, float inv_cap) {
+  float z = x;
+  float th = 0.0f;
+  if (cap) {
+    th = tanh_from_exp(__fmul_rn(z, inv_cap));
+    z = __fmul_rn(softcap, th);
+  }
+  const float p = fast_ex2(fmaf(z, kLog2e, -rc.x));
+  float g = __fmul_rn(p, fmaf(-rc.z, z, rc.y));
+  if (is_label) g = __fsub_rn(g, rc.w);
+  if (smooth) g = __fsub_rn(g, dw);
+  if (cap) g = __fmul_rn(g, fmaf(-th, th, 1.0f));
+  return g;
+}
+
 // dlogits of one row over its columns of the current vocabulary chunk.
 template <>
 struct Epilogue<EPI_DLOGITS> {
@@ -333,19 +365,12 @@ struct Epilogue<EPI_DLOGITS> {
         float g2[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float z = x[j + h];
-          float th = 0.0f;
-          if (cap) {
-            th = tanh_from_exp(z * inv_cap);
-            z = ea.softcap * th;
-          }
-          const float p = fast_ex2(fmaf(z, kLog2e, -rc.x));
-          float g = p * fmaf(-rc.z, z, rc.y);
-          if (vb + j + h == y) g -= rc.w;
-          if (smooth && j + h < nvalid)
-            g = fmaf(-dcoef, ea.cw ? __ldg(ea.cw + vb + j + h) : 1.0f, g);
-          if (cap) g *= fmaf(-th, th, 1.0f);
-          g2[h] = (j + h < nvalid) ? g : 0.0f;
+          const bool in = j + h < nvalid;
+          const float dw =
+              (smooth && in) ? __fmul_rn(dcoef, ea.cw ? __ldg(ea.cw + vb + j + h) : 1.0f) : 0.0f;
+          const float g = dlogit_of(x[j + h], rc, vb + j + h == y, smooth, dw, cap, ea.softcap,
+                                    inv_cap);
+          g2[h] = in ? g : 0.0f;
         }
         pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
       }
@@ -693,6 +718,7 @@ cudaError_t launch_pair_cached(const CUtensorMap& tmA, const CUtensorMap& tmB,
 FLCE_DECLARE_LAUNCHER(launch_fwd_stats);     // hidden (K) x weight (MN)
 FLCE_DECLARE_LAUNCHER(launch_bwd_dlogits);   // hidden (K) x weight (MN)
 FLCE_DECLARE_LAUNCHER(launch_bwd_dweight);   // hidden^T (MN) x dlogits (MN); also dlogits^T (MN) x hidden (MN)
+FLCE_DECLARE_LAUNCHER(launch_bwd_dweight_acc);  // the same, fp32-accumulated over token chunks
 FLCE_DECLARE_LAUNCHER(launch_bwd_dhidden);   // dlogits (K) x weight (K)
 // weight stored [V, H] (the nn.Linear layout)
 FLCE_DECLARE_LAUNCHER(launch_fwd_stats_vh);    // hidden (K) x weight (K)

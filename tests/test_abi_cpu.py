@@ -24,7 +24,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(flce_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_exported_set(lib):
@@ -35,22 +35,23 @@ def test_header_declares_the_exported_set(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.flce_version() == 100
+    assert lib.flce_version() == 200
     for code in range(0, 9):
         assert lib.flce_strerror(code)
     assert b"unknown" in lib.flce_strerror(99)
 
 
 def test_params_struct_layout():
-    # int64 x4, int32, float, float, int32, int64, int32, float, pointer, int64 x2
-    # -> 88 bytes, as in flce.h
-    assert ctypes.sizeof(B.FlceParams) == 88
+    # int64 x4, int32, float, float, int32, int64, int32, float, pointer, int64 x3
+    # -> 96 bytes, as in flce.h
+    assert ctypes.sizeof(B.FlceParams) == 96
     assert B.FlceParams.chunk_v.offset == 48
     assert B.FlceParams.weight_layout.offset == 56
     assert B.FlceParams.label_smoothing.offset == 60
     assert B.FlceParams.class_weight.offset == 64
     assert B.FlceParams.v_offset.offset == 72
     assert B.FlceParams.v_total.offset == 80
+    assert B.FlceParams.chunk_n.offset == 88
 
 
 def test_params_struct_matches_the_c_compiler(tmp_path):
@@ -59,16 +60,17 @@ def test_params_struct_matches_the_c_compiler(tmp_path):
     src = tmp_path / "t.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "flce.h"\n'
-        'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(flce_params),'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(flce_params),'
         ' offsetof(flce_params, chunk_v), offsetof(flce_params, class_weight),'
-        ' offsetof(flce_params, v_offset), offsetof(flce_params, v_total)); return 0;}\n')
+        ' offsetof(flce_params, v_offset), offsetof(flce_params, v_total),'
+        ' offsetof(flce_params, chunk_n)); return 0;}\n')
     exe = tmp_path / "t"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     F = B.FlceParams
     assert [int(x) for x in out] == [ctypes.sizeof(F), F.chunk_v.offset, F.class_weight.offset,
-                                     F.v_offset.offset, F.v_total.offset]
+                                     F.v_offset.offset, F.v_total.offset, F.chunk_n.offset]
 
 
 def test_workspace_sizes(lib):
@@ -86,6 +88,23 @@ def test_workspace_sizes(lib):
     assert flce.kernel_launches(flce.make_params(300, 200, 1000, "sum"), 0) == 3
 
 
+def test_fused_workspace_and_launches(lib):
+    # gradient in forward: fp32 logits + bf16 dlogits of one token chunk (auto: the
+    # Llama-3 head shape fits one chunk), no dweight accumulator for a single chunk
+    p = flce.make_params(8192, 4096, 128256, "mean", zloss_coef=1e-4)
+    ws = flce.workspace_size(p, 3)
+    assert 8192 * 128256 * 6 <= ws < 8192 * 128256 * 6 + (256 << 20)
+    assert flce.kernel_launches(p, 4) == 6 + 1
+    # explicit chunks of 512 rows: 3 chunks for 1100 rows, plus an fp32 dweight accumulator
+    p2 = flce.make_params(1100, 64, 1000, "none", chunk_n=512)
+    assert flce.workspace_size(p2, 3) >= 512 * 1024 * 6 + 64 * 1000 * 4
+    assert flce.kernel_launches(p2, 4) == 6 * 3
+    # one chunk when N fits: no accumulator
+    p3 = flce.make_params(300, 64, 1000, "sum", chunk_n=512)
+    assert flce.workspace_size(p3, 3) < 512 * 1024 * 6 + 64 * 1000 * 4
+    assert flce.kernel_launches(p3, 4) == 6 + 1
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(N=10, H=7 * 8 + 4, V=64), 3),     # H % 8
     (dict(N=10, H=64, V=100), 3),           # V % 8
@@ -93,6 +112,7 @@ def test_workspace_sizes(lib):
     (dict(N=-1, H=64, V=64), 2),
     (dict(N=10, H=64, V=0), 2),
     (dict(N=10, H=64, V=64, chunk_v=100), 1),
+    (dict(N=10, H=64, V=64, chunk_n=256), 1),               # chunk_n % 512
     (dict(N=10, H=64, V=64, zloss_coef=-1.0), 1),
     (dict(N=10, H=64, V=64, weight_layout=7), 1),
     (dict(N=10, H=64, V=64, label_smoothing=1.5), 1),
@@ -117,6 +137,36 @@ def test_bad_params_rejected_on_host(lib, kw, code):
     rc = lib.flce_backward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, fake,
                            fake, fake, 1 << 20, None)
     assert rc == code
+    assert lib.flce_workspace_size(ctypes.byref(p), 3) == 0
+    rc = lib.flce_forward_backward(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake,
+                                   fake, fake, fake, fake, fake, 1 << 20, None)
+    assert rc == code
+
+
+def test_fused_rejects_shards_nulls_alignment_and_small_workspace(lib):
+    ok = ctypes.c_void_p(0x10000)
+    bad = ctypes.c_void_p(0x10004)
+    # a partial vocabulary shard has no whole-vocabulary logsumexp to form dlogits with
+    p = flce.make_params(10, 64, 64, "mean", v_offset=64, v_total=128)
+    args = [ok] * 12
+    assert lib.flce_forward_backward(ctypes.byref(p), *args, 1 << 20, None) == 1
+    p = flce.make_params(10, 64, 64, "mean")
+    nulls = list(args)
+    nulls[9] = None  # dhidden
+    assert lib.flce_forward_backward(ctypes.byref(p), *nulls, 1 << 20, None) == 1
+    mis = list(args)
+    mis[10] = bad  # dweight
+    assert lib.flce_forward_backward(ctypes.byref(p), *mis, 1 << 20, None) == 3
+    assert lib.flce_forward_backward(ctypes.byref(p), *args, 16, None) == 4
+
+
+def test_scale_bf16_argument_checks(lib):
+    ok = ctypes.c_void_p(0x10000)
+    assert lib.flce_scale_bf16(ok, -1, ok, None) == 1
+    assert lib.flce_scale_bf16(ok, 8, None, None) == 1
+    assert lib.flce_scale_bf16(None, 8, ok, None) == 1
+    assert lib.flce_scale_bf16(ctypes.c_void_p(0x10002), 8, ok, None) == 3
+    assert lib.flce_scale_bf16(ok, 0, ok, None) == 0
 
 
 def test_bad_reduction_and_nulls(lib):
