@@ -41,7 +41,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_head")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-grad-in-forward", action="store_true",
                     help="skip timing the one-call forward+backward (gradient in forward)")
@@ -335,43 +335,46 @@ def run_ours(args):
                "gpu_launches": kernel_launches(p, 4) * K}
         del ws_g
 
-    # end to end: pinned host inputs -> device, fwd + bwd, loss/entropy back to host
-    hp = hidden.pin_memory()
-    Wp = weight.pin_memory()
-    yp = labels.pin_memory()
-    glp, gep = g_loss.pin_memory(), g_ent.pin_memory()
-    loss_h = torch.empty(n_out).pin_memory()
-    ent_h = torch.empty(n_out).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hp, Wp, yp, glp, gep))
-    d2h = 2 * n_out * 4
+    # end to end through HostPipeline: every step's inputs copied in from pinned host memory
+    # (on a side stream, the next step's copy overlapping this step's compute) and its loss and
+    # entropy copied back, all inside the timed region
+    from linear_cross_entropy_forward_gb300.pipeline import HostPipeline
+    host_in = (hidden.pin_memory(), weight.pin_memory(), labels.cpu().pin_memory(),
+               g_loss.pin_memory(), g_ent.pin_memory())
 
-    def e2e_step():
-        hd.copy_(hp, non_blocking=True)
-        Wd.copy_(Wp, non_blocking=True)
-        yd.copy_(yp, non_blocking=True)
-        gld.copy_(glp, non_blocking=True)
-        ged.copy_(gep, non_blocking=True)
-        fwd()
-        bwd()
-        loss_h.copy_(loss, non_blocking=True)
-        ent_h.copy_(ent, non_blocking=True)
+    def e2e(gif):
+        pipe = HostPipeline(N, H, V, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap,
+                            grad_in_forward=gif, device=dev)
+        pipe.submit(*host_in)
+        pipe.step()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        steps = args.e2e_steps
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pipe.copy_stream.wait_stream(stream)
+        pipe.submit(*host_in)
+        for i in range(steps):
+            if i + 1 < steps:
+                pipe.submit(*host_in)
+            pipe.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        if pg:
+            t = torch.tensor([ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+        res = (ms, pipe.h2d_bytes(), pipe.d2h_bytes())
+        del pipe
+        return res
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, h2d, d2h = e2e(False)
+    if gif is not None:
+        gms, _, _ = e2e(True)
+        gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms}
 
     ms_step = total_ms / K
     tokens = N * world

@@ -13,6 +13,7 @@ from ._binding import (FlceError, FlceParams, flce_backward, flce_combine_shards
                        flce_shard_stats, flce_status, kernel_launches,
                        linear_cross_entropy, load_library, make_params, workspace_size,
                        LIB_PATH, EXPORTED)
+from .pipeline import HostPipeline  # noqa: F401
 from .vocab_parallel import (exchange_stats, reduce_dhidden,  # noqa: F401
                              vocab_parallel_linear_cross_entropy)
 from .workloads import IGNORE_INDEX, WORKLOADS  # noqa: F401

@@ -611,10 +611,15 @@ int raster_group(int64_t panel_bytes, int fast_tiles) {
 
 // Two CTA pairs per cluster share one operand (halving its L2 requests): along a
 // dimension with an even tile count (no spare tile), else along the longer one; a
-// single tile keeps one pair per cluster.  `panel_bytes` is the revisited operand's
-// size per tile of the fast raster dimension; the group is counted in cluster tiles.
+// single tile keeps one pair per cluster.  Clusters of four fit fewer pairs at once
+// (144 of 152 SMs on GB300), so with FLCE_CLUSTER_SHARE 2 (the default) they are
+// used only when the persistent schedule needs at most 6 % more rounds of tiles than
+// with one pair per cluster: the halved L2 requests lower the power draw, which
+// under the power cap buys back about that much clock; 1 always shares, 0 never.  `panel_bytes` is the revisited
+// operand's size per tile of the fast raster dimension; the group is counted in
+// cluster tiles.
 #ifndef FLCE_CLUSTER_SHARE
-#define FLCE_CLUSTER_SHARE 1
+#define FLCE_CLUSTER_SHARE 2
 #endif
 void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
   int share = 0;
@@ -625,6 +630,14 @@ void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
       share = 2;
     else if (int64_t(sh->m_tiles) * sh->n_tiles > 1)
       share = sh->m_tiles >= sh->n_tiles ? 1 : 2;
+  }
+  if (share && FLCE_CLUSTER_SHARE == 2) {
+    const int64_t c4 = cluster_capacity(4), c2 = cluster_capacity(2);
+    const int64_t pair_tiles = int64_t(sh->m_tiles) * sh->n_tiles;
+    const int64_t quad_tiles = (share == 1 ? cdiv(sh->m_tiles, 2) * sh->n_tiles
+                                           : sh->m_tiles * cdiv(sh->n_tiles, 2));
+    if (c4 <= 0 || c2 <= 0 || cdiv(quad_tiles, c4) * 100 > cdiv(pair_tiles, c2) * 106)
+      share = 0;
   }
   sh->share = share;
   const bool m_fast = sh->raster == 0;

@@ -15,6 +15,15 @@
 #define FLCE_WAIT_LIMIT_NS 2000000000ull  // 2 s
 #endif
 
+// Upper bound (ns) on how long one mbarrier.try_wait may keep its thread suspended
+// before it re-checks.  Without it the suspended thread resumed well after the
+// phase completed: the producer / UMMA handshake then starved the tensor pipe
+// (~73 % busy on the forward GEMM instead of ~85 %).  Any value of 10-100 ns gives
+// the same cycles; a tight test_wait spin is slower (it takes issue slots).
+#ifndef FLCE_WAIT_HINT_NS
+#define FLCE_WAIT_HINT_NS 20
+#endif
+
 namespace flce {
 
 // Device error word bits (OR-ed into the workspace header).
@@ -53,10 +62,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(FLCE_WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -66,10 +75,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(FLCE_WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }

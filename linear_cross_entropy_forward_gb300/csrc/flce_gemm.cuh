@@ -705,6 +705,11 @@ cudaError_t launch_pair_cached(const CUtensorMap& tmA, const CUtensorMap& tmB,
   return launch_gemm_pair<EPI, A_MN, B_MN, TN>(tmA, tmB, sh, ea, mc, stream);
 }
 
+// Clusters of `csize` (2 or 4) CTAs that fit on the current device at once; every
+// pair kernel takes a whole SM's shared memory, so one query serves them all.
+// 0 if the query fails.
+int cluster_capacity(int csize);
+
 // Launchers of the instantiations the path uses (one translation unit each).
 #define FLCE_DECLARE_LAUNCHER(name)                                                  \
   cudaError_t name(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmShape& sh, \
