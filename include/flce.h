@@ -95,7 +95,8 @@ typedef struct {
   float zloss_coef;      /* z-loss coefficient, 0 = off */
   float softcap;         /* tanh logit soft-cap c, 0 = off */
   int32_t validate;      /* != 0: synchronise at the end and report device errors */
-  int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto */
+  int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto:
+                          * the widest whose bf16 dlogits [N, chunk_v] fit 1 GiB */
   int32_t weight_layout; /* flce_weight_layout: how weight and dweight are stored */
   float label_smoothing; /* eps in [0, 1], 0 = off */
   const float* class_weight; /* [V] fp32 device pointer, per-class target weights; NULL = all 1 */

@@ -34,7 +34,10 @@ namespace {
 constexpr int kVersion = 200;  // 0.2.0
 constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
-constexpr int64_t kDefaultChunkBytes = int64_t(256) << 20;  // dlogits chunk target
+// dlogits chunk target of the backward: fewer, wider chunks mean fewer fp32 passes
+// over the dhidden accumulator and longer k-loops (1 GB measured 3-4 % faster than
+// 256 MB on the Llama-3, Qwen2.5 and Gemma-2 head shapes)
+constexpr int64_t kDefaultChunkBytes = int64_t(1) << 30;
 
 // Descriptor strides of the MN-major operand tiles: 64-wide MN atoms 8 KB apart
 // (leading byte offset), 8-row K groups 1 KB apart (stride byte offset).
@@ -319,38 +322,64 @@ __global__ void __launch_bounds__(1024) bwd_prep_kernel(
 
 // dlogits [rows, ldz] (bf16) from the raw fp32 logits z [rows, ldz] the forward
 // GEMM kept, with the per-row constants of bwd_prep_kernel; the same per-element
-// arithmetic as the recompute epilogue (dlogit_of), zero beyond column V.
-__global__ void __launch_bounds__(256) dlogits_from_z_kernel(
+// arithmetic as the recompute epilogue (dlogit_of), zero beyond column V.  Each
+// thread converts two groups of 8 columns a block-width apart, issuing both groups'
+// loads first (the logits are read once: evict-first).
+constexpr int kDlzThreads = 256;
+constexpr int kDlzCols = 2 * 8 * kDlzThreads;  // columns per block
+
+__device__ __forceinline__ uint4 dlogits8(const float (&x)[8], int64_t c0, const float4& rc,
+                                          float dcoef, int64_t y, int64_t V, bool cap,
+                                          float softcap, float inv_cap, bool smooth,
+                                          const float* __restrict__ cw) {
+  uint32_t pk[4];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    float g2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t v = c0 + j + h;
+      const bool in = v < V;
+      const float dw = (smooth && in) ? __fmul_rn(dcoef, cw ? __ldg(cw + v) : 1.0f) : 0.0f;
+      const float g = dlogit_of(x[j + h], rc, v == y, smooth, dw, cap, softcap, inv_cap);
+      g2[h] = in ? g : 0.0f;
+    }
+    pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+  }
+  return make_uint4(pk[0], pk[1], pk[2], pk[3]);
+}
+
+__global__ void __launch_bounds__(kDlzThreads) dlogits_from_z_kernel(
     const float* __restrict__ z, int64_t rows, int64_t ldz, const float4* __restrict__ rowc,
     const float* __restrict__ rowd, const int64_t* __restrict__ labels, int64_t V,
     float softcap, int smooth, const float* __restrict__ cw, __nv_bfloat16* __restrict__ dl) {
-  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (c0 >= ldz) return;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kDlzCols + threadIdx.x * 8;
+  const int64_t c1 = c0 + kDlzThreads * 8;
+  const bool has0 = c0 < ldz, has1 = c1 < ldz;
+  if (!has0) return;
   const bool cap = softcap != 0.0f;
   const float inv_cap = cap ? 1.0f / softcap : 0.0f;
   for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const float* zr = z + row * ldz;
+    const float4 a0 = __ldcs(reinterpret_cast<const float4*>(zr + c0));
+    const float4 b0 = __ldcs(reinterpret_cast<const float4*>(zr + c0 + 4));
+    float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = a1;
+    if (has1) {
+      a1 = __ldcs(reinterpret_cast<const float4*>(zr + c1));
+      b1 = __ldcs(reinterpret_cast<const float4*>(zr + c1 + 4));
+    }
     const float4 rc = rowc[row];
     const float dcoef = smooth ? rowd[row] : 0.0f;
     const int64_t yl = labels[row];
     const int64_t y = (yl >= 0 && yl < V) ? yl : -1;
-    const float4 za = *reinterpret_cast<const float4*>(z + row * ldz + c0);
-    const float4 zb = *reinterpret_cast<const float4*>(z + row * ldz + c0 + 4);
-    const float x[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
-    uint32_t pk[4];
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      float g2[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t v = c0 + j + h;
-        const bool in = v < V;
-        const float dw = (smooth && in) ? __fmul_rn(dcoef, cw ? __ldg(cw + v) : 1.0f) : 0.0f;
-        const float g = dlogit_of(x[j + h], rc, v == y, smooth != 0, dw, cap, softcap, inv_cap);
-        g2[h] = in ? g : 0.0f;
-      }
-      pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+    const float x0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+    *reinterpret_cast<uint4*>(dl + row * ldz + c0) =
+        dlogits8(x0, c0, rc, dcoef, y, V, cap, softcap, inv_cap, smooth != 0, cw);
+    if (has1) {
+      const float x1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+      *reinterpret_cast<uint4*>(dl + row * ldz + c1) =
+          dlogits8(x1, c1, rc, dcoef, y, V, cap, softcap, inv_cap, smooth != 0, cw);
     }
-    *reinterpret_cast<uint4*>(dl + row * ldz + c0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -644,7 +673,24 @@ void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
   const int cm = share == 1 ? (sh->m_tiles + 1) / 2 : sh->m_tiles;
   const int cn = share == 2 ? (sh->n_tiles + 1) / 2 : sh->n_tiles;
   const bool fast_shared = m_fast ? share == 1 : share == 2;
-  sh->group = raster_group(panel_bytes * (fast_shared ? 2 : 1), m_fast ? cm : cn);
+  const int64_t panel = panel_bytes * (fast_shared ? 2 : 1);
+  const int fast = m_fast ? cm : cn;
+  // When few panels fit the L2 budget, a square-ish set of resident tiles reads
+  // fewer distinct rows and columns: the k-steps of all resident tiles advance
+  // together (persistent schedule), so only the k-slices in flight need to be in L2.
+  const int64_t cap = cluster_capacity(share ? 4 : 2);
+  int g = 1;
+  while (int64_t(g + 1) * (g + 1) <= cap) ++g;
+  const int budget_group = raster_group(panel, fast);
+  if (budget_group < g && budget_group < fast) {
+    sh->group = g < fast ? g : fast;
+    // No panel stays in L2 for long here: an evict_last policy would only pin
+    // hundreds of MB of lines that later loads (and later kernels) then miss around.
+    sh->a_hint = L2_NORMAL;
+    sh->b_hint = L2_NORMAL;
+  } else {
+    sh->group = budget_group;
+  }
 }
 
 GemmShape base_shape(int a_hint, int b_hint) {
@@ -1159,11 +1205,11 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
         p->class_weight, rowc, rowd);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
     {
-      const dim3 grid(static_cast<unsigned>(cdiv(L.ldz / 8, 256)),
+      const dim3 grid(static_cast<unsigned>(cdiv(L.ldz, kDlzCols)),
                       static_cast<unsigned>(rows < 65535 ? rows : 65535));
-      dlogits_from_z_kernel<<<grid, 256, 0, st>>>(so.zout, rows, L.ldz, rowc, rowd, lab, V,
-                                                  p->softcap, smooth ? 1 : 0, p->class_weight,
-                                                  dl);
+      dlogits_from_z_kernel<<<grid, kDlzThreads, 0, st>>>(
+          so.zout, rows, L.ldz, rowc, rowd, lab, V, p->softcap, smooth ? 1 : 0,
+          p->class_weight, dl);
       if ((rc = cuda_rc(cudaGetLastError()))) return rc;
     }
 
@@ -1182,7 +1228,6 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     s5.k_blocks = static_cast<int>(cdiv(V, BK));
     s5.raster = 0;
     plan_tiles(&s5, int64_t(PAIR_BM) * V * 2, TN_DHIDDEN);
-    s5.group = s5.share == 1 ? 4 : 8;
     EpiArgs e5{};
     e5.rows = static_cast<int>(rows);
     e5.cols = static_cast<int>(H);
