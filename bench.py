@@ -351,30 +351,31 @@ def run_ours(args):
         if pg:
             pg.barrier()
         steps = args.e2e_steps
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
         pipe.copy_stream.wait_stream(stream)
         pipe.submit(*host_in)
         for i in range(steps):
             if i + 1 < steps:
                 pipe.submit(*host_in)
             pipe.step()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
+        ms = ev[0].elapsed_time(ev[steps]) / steps
+        med = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
         if pg:
             t = torch.tensor([ms], device=dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             ms = float(t.item())
-        res = (ms, pipe.h2d_bytes(), pipe.d2h_bytes())
+        res = (ms, med, pipe.h2d_bytes(), pipe.d2h_bytes())
         del pipe
         return res
 
-    e2e_ms, h2d, d2h = e2e(False)
+    e2e_ms, e2e_med, h2d, d2h = e2e(False)
     if gif is not None:
-        gms, _, _ = e2e(True)
-        gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms}
+        gms, gmed, _, _ = e2e(True)
+        gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
+                      "median_step_ms": gmed}
 
     ms_step = total_ms / K
     tokens = N * world
@@ -410,7 +411,7 @@ def run_ours(args):
                    "workspace_bwd_bytes": int(ws_b.numel()),
                    "unfused_fp32_logits_bytes": int(N * V * 4)},
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "median_step_ms": e2e_med},
         "gpu_launches": launches,
         "clocks": clocks,
     }

@@ -330,7 +330,7 @@ constexpr int kDlzCols = 2 * 8 * kDlzThreads;  // columns per block
 
 __device__ __forceinline__ uint4 dlogits8(const float (&x)[8], int64_t c0, const float4& rc,
                                           float dcoef, int64_t y, int64_t V, bool cap,
-                                          float softcap, float inv_cap, bool smooth,
+                                          float softcap, float k, bool smooth,
                                           const float* __restrict__ cw) {
   uint32_t pk[4];
 #pragma unroll
@@ -341,7 +341,7 @@ __device__ __forceinline__ uint4 dlogits8(const float (&x)[8], int64_t c0, const
       const int64_t v = c0 + j + h;
       const bool in = v < V;
       const float dw = (smooth && in) ? __fmul_rn(dcoef, cw ? __ldg(cw + v) : 1.0f) : 0.0f;
-      const float g = dlogit_of(x[j + h], rc, v == y, smooth, dw, cap, softcap, inv_cap);
+      const float g = dlogit_of(x[j + h], rc, v == y, smooth, dw, cap, softcap, k);
       g2[h] = in ? g : 0.0f;
     }
     pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kDlzThreads) dlogits_from_z_kernel(
   const bool has0 = c0 < ldz, has1 = c1 < ldz;
   if (!has0) return;
   const bool cap = softcap != 0.0f;
-  const float inv_cap = cap ? 1.0f / softcap : 0.0f;
+  const float k = cap ? 2.0f * kLog2e / softcap : 0.0f;
   for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
     const float* zr = z + row * ldz;
     const float4 a0 = __ldcs(reinterpret_cast<const float4*>(zr + c0));
@@ -374,11 +374,11 @@ __global__ void __launch_bounds__(kDlzThreads) dlogits_from_z_kernel(
     const int64_t y = (yl >= 0 && yl < V) ? yl : -1;
     const float x0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
     *reinterpret_cast<uint4*>(dl + row * ldz + c0) =
-        dlogits8(x0, c0, rc, dcoef, y, V, cap, softcap, inv_cap, smooth != 0, cw);
+        dlogits8(x0, c0, rc, dcoef, y, V, cap, softcap, k, smooth != 0, cw);
     if (has1) {
       const float x1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
       *reinterpret_cast<uint4*>(dl + row * ldz + c1) =
-          dlogits8(x1, c1, rc, dcoef, y, V, cap, softcap, inv_cap, smooth != 0, cw);
+          dlogits8(x1, c1, rc, dcoef, y, V, cap, softcap, k, smooth != 0, cw);
     }
   }
 }

@@ -307,13 +307,14 @@ __device__ __forceinline__ float fast_rcp(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// tanh from the identity tanh(x) = sign(x) (1 - e^{-2|x|}) / (1 + e^{-2|x|}).
-// e^{-2|x|} lies in (0, 1], so nothing overflows; the absolute error stays near
-// one fp32 ulp of 1, which is what the capped logit c * tanh(x) needs.
-__device__ __forceinline__ float tanh_from_exp(float x) {
-  float t = fast_ex2(-2.0f * kLog2e * fabsf(x));
-  float r = (1.0f - t) * fast_rcp(1.0f + t);
-  return copysignf(r, x);
+// Soft-cap by one exponential and one reciprocal: tanh(a) = 1 - 2 / (1 + e^{2a}), so
+// with k = 2 log2e / c and r = 1 / (1 + 2^{k x}),  tanh(x / c) = 1 - 2r  and
+// c tanh(x / c) = c - 2c r.  2^{k x} overflowing to +inf gives r = 0 (z = c), and
+// underflowing gives r = 1 (z = -c); near x = 0 the absolute error stays near one
+// fp32 ulp of 1 times c.  The epilogues run this per logit; every instruction they
+// save is issue time the UMMA issuer on the same SM gets back.
+__device__ __forceinline__ float softcap_r(float x, float k) {
+  return fast_rcp(1.0f + fast_ex2(__fmul_rn(x, k)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

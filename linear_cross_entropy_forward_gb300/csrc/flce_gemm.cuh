@@ -234,7 +234,9 @@ struct Epilogue<EPI_FWD_STATS> {
       if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
     }
     const bool cap = ea.softcap != 0.0f;
-    const float inv_cap = cap ? 1.0f / ea.softcap : 0.0f;
+    const float c = ea.softcap;
+    const float k = cap ? 2.0f * kLog2e / c : 0.0f;
+    const float c_l2 = c * kLog2e, m2c_l2 = -2.0f * c * kLog2e;
     const int vcol0 = ea.col_base + col0;
     const bool smooth = ea.smooth != 0.0f;
     float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f, sw = 0.0f;
@@ -242,38 +244,48 @@ struct Epilogue<EPI_FWD_STATS> {
     float* zrow = (ea.zout && row_ok) ? ea.zout + static_cast<int64_t>(row) * ea.ld_z + col0
                                       : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < CH; ++c) {
+    for (int ch = 0; ch < CH; ++ch) {
       float x[32];
-      tmem_ld32(tbase + c * 32, x);
-      const int vb = vcol0 + c * 32;
+      tmem_ld32(tbase + ch * 32, x);
+      const int vb = vcol0 + ch * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
       if (zrow) {
-        float4* z4 = reinterpret_cast<float4*>(zrow + c * 32);
+        float4* z4 = reinterpret_cast<float4*>(zrow + ch * 32);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           z4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
       }
-      if (cap) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = ea.softcap * tanh_from_exp(x[j] * inv_cap);
-      }
-      if (smooth) {
+      // the label's logit (natural units), from the one chunk that holds it
+      if (static_cast<unsigned>(y - vb) < 32u) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
+          if (j == y - vb) zy = cap ? fmaf(-2.0f * c, softcap_r(x[j], k), c) : x[j];
+        hit = true;
       }
-      float cm = -1e30f;
+      // logits in log2 units (capped), and the smoothing sum of w_v z_v
+      if (cap) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float z = x[j];
-        if (vb + j == y) {
-          zy = z;
-          hit = true;
+        for (int j = 0; j < 32; ++j) {
+          const float r = softcap_r(x[j], k);
+          if (smooth && j < nvalid)
+            sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, fmaf(-2.0f * c, r, c), sw);
+          x[j] = fmaf(m2c_l2, r, c_l2);
         }
-        float u = (j < nvalid) ? z * kLog2e : -1e30f;
-        x[j] = u;
-        cm = fmaxf(cm, u);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (smooth && j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
+          x[j] *= kLog2e;
+        }
       }
+      if (nvalid < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j >= nvalid) x[j] = -1e30f;
+      }
+      float cm = x[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
       if (cm > mx) {
         const float a = fast_ex2(mx - cm);
         s = a * fmaf(mx - cm, d, s);
@@ -315,13 +327,13 @@ struct Epilogue<EPI_FWD_STATS> {
 //   z = c tanh(x / c) (soft-cap, c != 0),  p = 2^{z log2e - lse log2e},
 //   g = p (A1 - b z) - C_y [v == y] - D w_v,  times 1 - tanh^2 under the cap.
 // Products that feed a sum are rounded explicitly, so every caller (the GEMM
-// epilogue, the gradient-in-forward kernel) gets the same bits.
+// epilogue, the gradient-in-forward kernel) gets the same bits.  k = 2 log2e / c.
 __device__ __forceinline__ float dlogit_of(float x, const float4& rc, bool is_label, bool smooth,
-                                           float dw, bool cap, float softcap, float inv_cap) {
+                                           float dw, bool cap, float softcap, float k) {
   float z = x;
   float th = 0.0f;
   if (cap) {
-    th = tanh_from_exp(__fmul_rn(z, inv_cap));
+    th = fmaf(-2.0f, softcap_r(x, k), 1.0f);
     z = __fmul_rn(softcap, th);
   }
   const float p = fast_ex2(fmaf(z, kLog2e, -rc.x));
@@ -350,32 +362,44 @@ struct Epilogue<EPI_DLOGITS> {
       if (yl >= 0 && yl < ea.V) y = static_cast<int>(yl);
     }
     const bool cap = ea.softcap != 0.0f;
-    const float inv_cap = cap ? 1.0f / ea.softcap : 0.0f;
+    const float k = cap ? 2.0f * kLog2e / ea.softcap : 0.0f;
     const int vcol0 = ea.col_base + col0;
     __nv_bfloat16* dst = ea.dl + static_cast<int64_t>(row) * ea.ld_dl + col0;
 #pragma unroll 1
-    for (int c = 0; c < CH; ++c) {
+    for (int ch = 0; ch < CH; ++ch) {
       float x[32];
-      tmem_ld32(tbase + c * 32, x);
-      const int vb = vcol0 + c * 32;
+      tmem_ld32(tbase + ch * 32, x);
+      const int vb = vcol0 + ch * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
-      uint32_t pk[16];
+      const int jy = static_cast<unsigned>(y - vb) < 32u ? y - vb : -1;  // label column, if here
+      float g[32];
+      if (!smooth && nvalid >= 32) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float g2[2];
+        for (int j = 0; j < 32; ++j) g[j] = dlogit_of(x[j], rc, false, false, 0.0f, cap, ea.softcap, k);
+      } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const bool in = j + h < nvalid;
+        for (int j = 0; j < 32; ++j) {
+          const bool in = j < nvalid;
           const float dw =
-              (smooth && in) ? __fmul_rn(dcoef, ea.cw ? __ldg(ea.cw + vb + j + h) : 1.0f) : 0.0f;
-          const float g = dlogit_of(x[j + h], rc, vb + j + h == y, smooth, dw, cap, ea.softcap,
-                                    inv_cap);
-          g2[h] = in ? g : 0.0f;
+              (smooth && in) ? __fmul_rn(dcoef, ea.cw ? __ldg(ea.cw + vb + j) : 1.0f) : 0.0f;
+          const float gj = dlogit_of(x[j], rc, false, smooth, dw, cap, ea.softcap, k);
+          g[j] = in ? gj : 0.0f;
         }
-        pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+      }
+      if (jy >= 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j == jy) {
+            const float dw = smooth ? __fmul_rn(dcoef, ea.cw ? __ldg(ea.cw + vb + j) : 1.0f) : 0.0f;
+            g[j] = dlogit_of(x[j], rc, true, smooth, dw, cap, ea.softcap, k);
+          }
+        }
       }
       if (row_ok) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
