@@ -264,19 +264,34 @@ struct Epilogue<EPI_FWD_STATS> {
       }
       // logits in log2 units (capped), and the smoothing sum of w_v z_v
       if (cap) {
+        const uint64_t k2 = f2_pack(k, k), one2 = f2_pack(1.0f, 1.0f);
+        const uint64_t a2 = f2_pack(m2c_l2, m2c_l2), b2 = f2_pack(c_l2, c_l2);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float r = softcap_r(x[j], k);
-          if (smooth && j < nvalid)
-            sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, fmaf(-2.0f * c, r, c), sw);
-          x[j] = fmaf(m2c_l2, r, c_l2);
+        for (int j = 0; j < 32; j += 2) {
+          // the lanes of softcap_r, two at a time
+          float e0, e1, r0, r1;
+          f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), k2), e0, e1);
+          f2_unpack(f2_add(one2, f2_pack(fast_ex2(e0), fast_ex2(e1))), r0, r1);
+          r0 = fast_rcp(r0);
+          r1 = fast_rcp(r1);
+          if (smooth) {
+            if (j < nvalid)
+              sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, fmaf(-2.0f * c, r0, c), sw);
+            if (j + 1 < nvalid)
+              sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j + 1) : 1.0f, fmaf(-2.0f * c, r1, c), sw);
+          }
+          f2_unpack(f2_fma(a2, f2_pack(r0, r1), b2), x[j], x[j + 1]);
         }
       } else {
+        if (smooth) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (smooth && j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
-          x[j] *= kLog2e;
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
         }
+        const uint64_t l2 = f2_pack(kLog2e, kLog2e);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), l2), x[j], x[j + 1]);
       }
       if (nvalid < 32) {
 #pragma unroll
@@ -293,13 +308,23 @@ struct Epilogue<EPI_FWD_STATS> {
         mx = cm;
       }
       if (nvalid >= 32) {
+        // two lanes of (d, s) per chunk, added into the running sums at its end
+        const uint64_t nmx = f2_pack(-mx, -mx);
+        uint64_t dd = f2_pack(0.0f, 0.0f), ss = dd;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float t = x[j] - mx;
-          const float e = fast_ex2(t);
-          d += e;
-          s = fmaf(e, t, s);
+        for (int j = 0; j < 32; j += 2) {
+          const uint64_t t = f2_add(f2_pack(x[j], x[j + 1]), nmx);
+          float t0, t1;
+          f2_unpack(t, t0, t1);
+          const uint64_t e = f2_pack(fast_ex2(t0), fast_ex2(t1));
+          dd = f2_add(dd, e);
+          ss = f2_fma(e, t, ss);
         }
+        float d0, d1, s0, s1;
+        f2_unpack(dd, d0, d1);
+        f2_unpack(ss, s0, s1);
+        d += d0 + d1;
+        s += s0 + s1;
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -344,6 +369,28 @@ __device__ __forceinline__ float dlogit_of(float x, const float4& rc, bool is_la
   return g;
 }
 
+// dlogit_of for two logits that are neither the label nor under label smoothing,
+// with the packed f32x2 arithmetic: lane by lane the same operations, so the same
+// bits as two calls of dlogit_of.
+__device__ __forceinline__ void dlogit_of2(float x0, float x1, const float4& rc, bool cap,
+                                           float softcap, float k, float& g0, float& g1) {
+  const uint64_t one2 = f2_pack(1.0f, 1.0f);
+  uint64_t z = f2_pack(x0, x1), th = 0;
+  if (cap) {
+    float e0, e1, r0, r1;
+    f2_unpack(f2_mul(z, f2_pack(k, k)), e0, e1);
+    f2_unpack(f2_add(one2, f2_pack(fast_ex2(e0), fast_ex2(e1))), r0, r1);
+    th = f2_fma(f2_pack(-2.0f, -2.0f), f2_pack(fast_rcp(r0), fast_rcp(r1)), one2);
+    z = f2_mul(f2_pack(softcap, softcap), th);
+  }
+  float q0, q1;
+  f2_unpack(f2_fma(z, f2_pack(kLog2e, kLog2e), f2_pack(-rc.x, -rc.x)), q0, q1);
+  const uint64_t p = f2_pack(fast_ex2(q0), fast_ex2(q1));
+  uint64_t g = f2_mul(p, f2_fma(f2_pack(-rc.z, -rc.z), z, f2_pack(rc.y, rc.y)));
+  if (cap) g = f2_mul(g, f2_fma(th ^ 0x8000000080000000ull, th, one2));
+  f2_unpack(g, g0, g1);
+}
+
 // dlogits of one row over its columns of the current vocabulary chunk.
 template <>
 struct Epilogue<EPI_DLOGITS> {
@@ -375,7 +422,8 @@ struct Epilogue<EPI_DLOGITS> {
       float g[32];
       if (!smooth && nvalid >= 32) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) g[j] = dlogit_of(x[j], rc, false, false, 0.0f, cap, ea.softcap, k);
+        for (int j = 0; j < 32; j += 2)
+          dlogit_of2(x[j], x[j + 1], rc, cap, ea.softcap, k, g[j], g[j + 1]);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
