@@ -198,6 +198,15 @@ int flce_status(const void* workspace, void* stream);
  * 4 flce_forward_backward; -1 when invalid. */
 int flce_kernel_launches(const flce_params* params, int phase);
 
+/* Self-test of the device-side failure detection (no counterpart on the pages): one
+ * kernel thread waits, with the bounded wait every pipeline kernel uses, on an
+ * mbarrier that nothing arrives on, gives up after limit_ns of global time
+ * (0 < limit_ns <= 2 s) and records the timeout in the workspace header, then returns.
+ * Afterwards flce_status(workspace, stream) reports FLCE_ERR_TIMEOUT and the CUDA
+ * context stays usable.  workspace: >= 256 bytes, 256-byte aligned.  Returns
+ * FLCE_OK once the kernel is enqueued (the timeout is the expected outcome). */
+int flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* flce_strerror(int code);
 

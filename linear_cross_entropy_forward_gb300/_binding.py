@@ -57,7 +57,7 @@ _lock = threading.Lock()
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
             "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc",
             "flce_shard_stats", "flce_combine_shards", "flce_forward_backward",
-            "flce_scale_bf16")
+            "flce_scale_bf16", "flce_selftest_wait_timeout")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flce_forward_backward.restype = ctypes.c_int
         lib.flce_scale_bf16.argtypes = [vp, ctypes.c_int64, vp, vp]
         lib.flce_scale_bf16.restype = ctypes.c_int
+        lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint64, vp]
+        lib.flce_selftest_wait_timeout.restype = ctypes.c_int
         lib.flce_version.argtypes = []
         lib.flce_version.restype = ctypes.c_int
         _lib = lib
@@ -338,6 +340,15 @@ def flce_combine_shards(stats, labels, v_total, reduction="mean", ignore_index=I
                                    _ptr(ent), _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
                                    _stream(stream)))
     return loss, ent, lse, ez
+
+
+def selftest_wait_timeout(limit_ns=20_000_000, stream=None) -> int:
+    """Run the bounded-wait self-test (a wait that nothing satisfies, given up after
+    limit_ns) and return the status flce_status then reads (FLCE_ERR_TIMEOUT = 6)."""
+    lib = load_library()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    _check(lib.flce_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_ns), _stream(stream)))
+    return flce_status(ws, stream)
 
 
 def flce_status(workspace, stream=None) -> int:

@@ -408,6 +408,20 @@ __global__ void __launch_bounds__(256) scale_bf16_kernel(__nv_bfloat16* __restri
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing will
+// ever arrive on, with the pipeline kernels' own wait, until `limit_ns` of global
+// time has passed; the wait then records FLCE_DEVERR_TIMEOUT in the error word and
+// the kernel returns, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+
 // ------------------------------------------------------------ host helpers
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -1302,6 +1316,20 @@ int flce_scale_bf16(void* x, int64_t n, const float* g, void* stream) {
   scale_bf16_kernel<<<static_cast<unsigned>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256,
                       0, static_cast<cudaStream_t>(stream)>>>(static_cast<__nv_bfloat16*>(x), n,
                                                               g);
+  return cuda_rc(cudaGetLastError());
+}
+
+int flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns,
+                                void* stream) {
+  using namespace flce;
+  if (!workspace) return FLCE_ERR_BAD_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return FLCE_ERR_ALIGN;
+  if (limit_ns == 0 || limit_ns > FLCE_WAIT_LIMIT_NS) return FLCE_ERR_BAD_ARG;
+  cudaStream_t st;
+  uint32_t* err;
+  int rc = begin_call(workspace, ws_bytes, kHeaderBytes, stream, &st, &err);
+  if (rc) return rc;
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
   return cuda_rc(cudaGetLastError());
 }
 

@@ -88,7 +88,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // role of the CTA has already aborted (*abort != 0).
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* err) {
+                                          uint32_t* err, uint64_t limit_ns = FLCE_WAIT_LIMIT_NS) {
   auto try_once = [&]() {
     return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -99,7 +99,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (try_once()) return true;
     if (((++spins) & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > FLCE_WAIT_LIMIT_NS) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         if (err) atomicOr(err, FLCE_DEVERR_TIMEOUT);
         return false;

@@ -198,3 +198,12 @@ def test_product_path_fails_loudly_without_library(tmp_path):
             B.load_library(str(tmp_path / "nope.so"))
     finally:
         B._lib = saved
+
+
+def test_selftest_wait_timeout_argument_checks(lib):
+    ok = ctypes.c_void_p(0x10000)
+    assert lib.flce_selftest_wait_timeout(None, 256, 1000, None) == 1
+    assert lib.flce_selftest_wait_timeout(ctypes.c_void_p(0x10010), 256, 1000, None) == 3
+    assert lib.flce_selftest_wait_timeout(ok, 256, 0, None) == 1
+    assert lib.flce_selftest_wait_timeout(ok, 256, 3_000_000_000, None) == 1
+    assert lib.flce_selftest_wait_timeout(ok, 16, 1000, None) == 4
