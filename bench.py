@@ -43,6 +43,8 @@ def parse_args():
     ap.add_argument("--workload", default="llama3_8b_head")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused-memory", action="store_true",
+                    help="skip measuring the unfused PyTorch baseline's peak memory")
     ap.add_argument("--no-grad-in-forward", action="store_true",
                     help="skip timing the one-call forward+backward (gradient in forward)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -215,6 +217,41 @@ def load_traffic(workload):
         return None
 
 
+def unfused_memory(torch, w, hd, Wd, yd, gld, ged, dev):
+    """Peak bytes the unfused computation allocates above its inputs (gradients, the
+    outputs both paths produce, excluded): logits in fp32 from fp32 copies of hidden
+    and weight, log-softmax, entropy and cross-entropy as written out on the pages,
+    z-loss and soft-cap when the workload has them, and autograd's backward."""
+    import torch.nn.functional as F
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    h = hd.detach().requires_grad_(True)
+    W = Wd.detach().requires_grad_(True)
+    logits = torch.matmul(h.float(), W.float())
+    if w.softcap:
+        logits = w.softcap * torch.tanh(logits / w.softcap)
+    lse = torch.logsumexp(logits, dim=-1)
+    p = torch.softmax(logits, dim=-1)
+    ent = lse - (p * logits).sum(-1)
+    ce = F.cross_entropy(logits, yd, ignore_index=-100, reduction="none")
+    valid = (yd != -100).float()
+    loss_t = (ce + w.zloss_coef * lse * lse) * valid
+    ent_t = ent * valid
+    if w.reduction == "none":
+        obj = (loss_t * gld).sum() + (ent_t * ged).sum()
+    else:
+        den = valid.sum() if w.reduction == "mean" else 1.0
+        obj = (loss_t.sum() * gld[0] + ent_t.sum() * ged[0]) / den
+    obj.backward()
+    torch.cuda.synchronize()
+    grads = h.grad.numel() * h.grad.element_size() + W.grad.numel() * W.grad.element_size()
+    peak = torch.cuda.max_memory_allocated(dev) - base - grads
+    del h, W, logits, lse, p, ent, ce, valid, loss_t, ent_t, obj
+    torch.cuda.empty_cache()
+    return int(peak)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -252,6 +289,10 @@ def run_ours(args):
     dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
     dw = torch.empty(H, V, dtype=torch.bfloat16, device=dev)
     p = make_params(N, H, V, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap)
+    # memory above the inputs, outputs and saved per-row statistics: the workspaces
+    torch.cuda.synchronize()
+    mem_base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     ws_f = torch.empty(workspace_size(p, 0), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(workspace_size(p, 1), dtype=torch.uint8, device=dev)
     kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
@@ -263,9 +304,10 @@ def run_ours(args):
         flce_backward(hd, Wd, yd, lse, ez, gld, ged, w.reduction, workspace=ws_b, out=(dh, dw),
                       **kw)
 
+    fwd()
+    bwd()
     torch.cuda.synchronize()
-    mem0 = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
+    peak_extra = torch.cuda.max_memory_allocated(dev) - mem_base
     sampler = ClockSampler(nvsmi_id(torch, local))
     for _ in range(args.warmup):
         fwd()
@@ -300,7 +342,6 @@ def run_ours(args):
         pg.barrier()
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
-    peak_extra = torch.cuda.max_memory_allocated(dev) - mem0
 
     # the same step as one flce_forward_backward call (gradient in forward, no recompute)
     gif = None
@@ -377,6 +418,14 @@ def run_ours(args):
         gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
                       "median_step_ms": gmed}
 
+    # the unfused baseline's memory: the pages' equivalent compute logic in plain PyTorch
+    # (fp32 logits, softmax, entropy, cross-entropy, autograd backward), run once outside
+    # every timed region; bytes above the inputs, the gradients excluded as outputs
+    unfused_peak = None
+    if not args.no_unfused_memory:
+        del ws_f, ws_b
+        unfused_peak = unfused_memory(torch, w, hd, Wd, yd, gld, ged, dev)
+
     ms_step = total_ms / K
     tokens = N * world
     value = tokens / (ms_step / 1e3)
@@ -407,8 +456,9 @@ def run_ours(args):
                           "unit": "TFLOP/s", "frac": tflops / peak,
                           "algorithmic": "8*N*H*V flops per step (fwd 2, bwd 6 incl. recompute)"},
         "memory": {"peak_extra_bytes": int(peak_extra),
-                   "workspace_fwd_bytes": int(ws_f.numel()),
-                   "workspace_bwd_bytes": int(ws_b.numel()),
+                   "unfused_peak_extra_bytes": unfused_peak,
+                   "workspace_fwd_bytes": int(workspace_size(p, 0)),
+                   "workspace_bwd_bytes": int(workspace_size(p, 1)),
                    "unfused_fp32_logits_bytes": int(N * V * 4)},
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "median_step_ms": e2e_med},
@@ -418,6 +468,8 @@ def run_ours(args):
     if gif is not None:
         gif["speedup_vs_two_call"] = ms_step / gif["ms_per_step"]
         out["grad_in_forward"] = gif
+    if gif is not None:
+        out["memory"]["grad_in_forward_extra_bytes"] = gif["workspace_bytes"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
                                            args.cpu_seconds)
