@@ -138,3 +138,30 @@ def test_llama2_head_against_complete_oracle():
     assert np.abs(f64(lse) - o["lse"]).max() <= TOK_ABS
     assert rel_l2(f64(dh), dh_o) <= GRAD_REL_L2
     assert rel_l2(f64(dw), dw_o) <= GRAD_REL_L2
+
+
+def test_fullsize_weight_layouts_agree_bitwise():
+    """Gemma-2 head shape (soft-cap 30, V = 256000): the nn.Linear layout [V,H] gives the
+    same bits as [H,V] for every output (the layouts change operand majorness and tile
+    order, never the order of any element's accumulation)."""
+    _cuda_or_skip()
+    w = wl.GEMMA2
+    dev = torch.device("cuda")
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    hd, yd, gl, ge = hidden.to(dev), labels.to(dev), g_loss.to(dev), g_ent.to(dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+    res = {}
+    for layout in ("hv", "vh"):
+        Wd = weight.to(dev) if layout == "hv" else weight.t().contiguous().to(dev)
+        loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True,
+                                          weight_layout=layout, **kw)
+        dh, dw = flce_backward(hd, Wd, yd, lse, ez, gl, ge, w.reduction, validate=True,
+                               weight_layout=layout, **kw)
+        torch.cuda.synchronize()
+        res[layout] = (loss, ent, lse, ez, dh, (dw if layout == "hv" else dw.t()).contiguous())
+        del Wd
+    for a, b in zip(res["hv"], res["vh"]):
+        if a.dtype == torch.bfloat16:
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        else:
+            assert torch.equal(a, b)
