@@ -8,27 +8,32 @@
 //               completion is counted on the pair leader's (even rank) full barrier.
 //   warp 1      UMMA issuer (leader only): 256 x TN x 16 tcgen05.mma.cta_group::2
 //               into one of 512/TN fp32 TMEM accumulators, commits multicast to
-//               the barriers of both CTAs.
-// A cluster holds one pair, or two pairs whose tiles lie side by side along M
-// (then they read the same B columns) or along N (the same A rows).  The shared
-// operand is fetched once per cluster: each CTA loads half of its 128-row share
-// and multicasts it to its counterpart in the other pair, which halves that
-// operand's L2 requests; a stage is released only when both pairs' UMMAs are done.
+//               the barriers of the cluster's CTAs.
 //   warps 2..9  epilogue (both CTAs): tcgen05.ld one row per thread (warp w reads
 //               TMEM lanes 32*(w%4)..+31 and column half (w-2)/4 of the tile),
 //               then one of:
 //     EPI_FWD_STATS  online-softmax partials per row and TN/2-column block:
 //                    running max m, sum-exp d and centred s = sum e^{u-m}(u-m)
 //                    in log2 units, plus the label logit (Liger-Kernel PR #551:
-//                    m and d of the online softmax feed the entropy).
+//                    m and d of the online softmax feed the entropy); optionally
+//                    also the raw fp32 logits (gradient in forward).
 //     EPI_DLOGITS    recomputed logits -> dlogits (bf16) of the CE, z-loss and
 //                    entropy terms, with the soft-cap chain rule (Liger-Kernel
 //                    issue #127: tanh capping after the matmul).
 //     EPI_STORE_BF16 plain bf16 store (dweight tiles).
-//     EPI_ACCUM      fp32 split-V accumulation of dhidden; last chunk -> bf16.
+//     EPI_ACCUM      fp32 accumulation across vocabulary chunks (dhidden) or token
+//                    chunks (dweight); the last chunk writes bf16.
 //
-// Operand majorness is a template choice: K-major tiles come in as one TMA box
-// {64, rows}; MN-major tiles as rows/64 boxes {64, 64} stacked 8 KB apart.
+// A cluster holds one pair, or two pairs whose tiles lie side by side along M
+// (then they read the same B columns) or along N (the same A rows).  The shared
+// operand is fetched once per cluster: each CTA loads half of its 128-row share
+// and multicasts it to its counterpart in the other pair, which halves that
+// operand's L2 requests; a stage is released only when both pairs' UMMAs are done.
+//
+// Operands arrive as 64-row pieces of 8 KB ({64 K, 64 rows} boxes for K-major,
+// {64 MN, 64 K} boxes of the transposed view for MN-major); operand majorness is a
+// template choice, so no transposed copy of any tensor is made.  Every barrier
+// wait is bounded (flce_device.cuh).
 #pragma once
 
 #include <atomic>
