@@ -530,11 +530,13 @@ struct Epilogue<EPI_ACCUM> {
 };
 
 // ------------------------------------------------------------------ pair kernel
-// Both producers load their halves; completion is counted on the leader's full
-// barrier, which expects both CTAs' bytes.  The leader's UMMA warp commits to the
-// empty / tmem-full barriers of both CTAs at once (multicast).  Each CTA's
-// epilogue reads its own 128 TMEM lanes (rows) and arrives on the leader's
-// tmem-empty barrier.
+// Both producers of a pair load their halves (or, with two pairs per cluster, half of
+// the shared operand's share each, multicast to the other pair); completion is
+// counted on the pair leader's full barrier, which expects the bytes landing in both
+// of its CTAs.  Each leader's UMMA warp commits to the empty barriers of every CTA of
+// the cluster (a stage is free once every pair is done with it) and to the
+// tmem-full barriers of its own pair.  Each CTA's epilogue reads its own 128 TMEM
+// lanes (rows) and arrives on its pair leader's tmem-empty barrier.
 template <int EPI, bool A_MN, bool B_MN, int TN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
