@@ -71,6 +71,11 @@ def test_fullsize_sampled_parity(w):
     for name, arr in (("lse", g_lse), ("ez", g_ez), ("loss", g_lt), ("ent", g_et)):
         assert np.all(np.isfinite(arr)), name
     assert np.all(g_lt[~valid] == 0) and np.all(g_et[~valid] == 0)
+    # entropy of a softmax over V classes lies in [0, ln V]; cross-entropy is >= 0
+    # (loose fp32 margins: the bounds are attained only in the limit)
+    assert np.all(g_et[valid] >= -1e-5) and np.all(g_et[valid] <= np.log(w.V) + 1e-4)
+    if w.zloss_coef == 0:
+        assert np.all(g_lt[valid] >= -1e-5)
 
     # reduced outputs are the mean / sum of the per-token outputs (property at any size)
     if w.reduction != "none":
