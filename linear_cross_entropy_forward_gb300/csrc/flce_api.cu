@@ -58,7 +58,7 @@ constexpr size_t kWsumOffset = 64;  // float in the workspace header: sum of cla
 
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
-  L.n_parts = 2 * cdiv(p->V, TN_FWD);  // one part per TN_FWD/2 columns
+  L.n_parts = PairCfg<TN_FWD, epi_warps<EPI_FWD_STATS>()>::PARTS * cdiv(p->V, TN_FWD);  // one part per warp's columns
   const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * p->N) * 4);
   const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
   size_t off = kHeaderBytes;
@@ -128,7 +128,7 @@ FusedLayout fused_layout(const flce_params* p) {
   const int64_t ncap = cdiv(p->N > 0 ? p->N : 1, 256) * 256;
   L.Nc = nc < ncap ? nc : ncap;
   L.chunks = cdiv(p->N, L.Nc);
-  L.n_parts = 2 * cdiv(p->V, TN_FWD);
+  L.n_parts = PairCfg<TN_FWD, epi_warps<EPI_FWD_STATS>()>::PARTS * cdiv(p->V, TN_FWD);
   const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * L.Nc) * 4);
   const size_t chunk_row_bytes = align256(static_cast<size_t>(L.Nc) * 4);
   const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);

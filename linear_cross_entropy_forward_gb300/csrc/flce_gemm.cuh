@@ -9,10 +9,10 @@
 //   warp 1      UMMA issuer (leader only): 256 x TN x 16 tcgen05.mma.cta_group::2
 //               into one of 512/TN fp32 TMEM accumulators, commits multicast to
 //               the barriers of the cluster's CTAs.
-//   warps 2..9  epilogue (both CTAs): tcgen05.ld one row per thread (warp w reads
-//               TMEM lanes 32*(w%4)..+31 and column half (w-2)/4 of the tile),
-//               then one of:
-//     EPI_FWD_STATS  online-softmax partials per row and TN/2-column block:
+//   warps 2..   epilogue (both CTAs, 4 or 8 warps, see epi_warps): tcgen05.ld one
+//               row per thread (warp w reads TMEM lanes 32*(w%4)..+31 and, with 8
+//               warps, column half (w-2)/4 of the tile), then one of:
+//     EPI_FWD_STATS  online-softmax partials per row and warp column block:
 //                    running max m, sum-exp d and centred s = sum e^{u-m}(u-m)
 //                    in log2 units, plus the label logit (Liger-Kernel PR #551:
 //                    m and d of the online softmax feed the entropy); optionally
@@ -45,8 +45,24 @@ namespace flce {
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int UK = 16;  // K of one kind::f16 UMMA
 constexpr int PAIR_BM = 256;  // rows of a pair tile (128 per CTA)
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+enum EpiKind { EPI_FWD_STATS = 0, EPI_DLOGITS = 1, EPI_STORE_BF16 = 2, EPI_ACCUM = 3 };
+
+// Epilogue warps per CTA: 4 (one per TMEM lane quadrant, all of a tile's columns)
+// or 8 (two per quadrant, half the columns each).  Epilogue arithmetic costs the
+// UMMA issuer issue slots, so fewer warps are better where the epilogue of a tile
+// stays well inside the next tile's mainloop; the dlogits epilogue (with the
+// soft-cap, on tiles of only H/64 k-steps) needs 8 to stay hidden.
+#ifndef FLCE_EPI_WARPS
+#define FLCE_EPI_WARPS 0  // 0: per epilogue kind as below; 4 or 8: every kind
+#endif
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() {
+  return FLCE_EPI_WARPS ? FLCE_EPI_WARPS : (EPI == EPI_DLOGITS ? 8 : 4);
+}
+template <int EPI>
+__host__ __device__ constexpr int pair_threads() {
+  return 64 + 32 * epi_warps<EPI>();
+}
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // one {64 MN x 64 K} box
 constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
@@ -55,8 +71,8 @@ constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
 #define FLCE_MAX_STAGES 9
 #endif
 
-// Per-tile-width configuration of the pair kernel.
-template <int TN>
+// Per-tile-width (and epilogue-warp-count) configuration of the pair kernel.
+template <int TN, int EW>
 struct PairCfg {
   static_assert(TN == 128 || TN == 256, "tile width");
   static constexpr int B_ROWS = TN / 2;                // this CTA's share of B's columns
@@ -64,8 +80,10 @@ struct PairCfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;      // 8 or 16 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int NACC = TMEM_COLS / TN;          // TMEM accumulators
-  static constexpr int EPI_COLS = TN / 2;              // columns per epilogue warp
+  static_assert(EW == 4 || EW == 8, "epilogue warps");
+  static constexpr int EPI_COLS = TN * 4 / EW;          // columns per epilogue warp
   static constexpr int EPI_CHUNKS = EPI_COLS / 32;     // tcgen05.ld x32 per warp per tile
+  static constexpr int PARTS = TN / EPI_COLS;           // statistics parts per tile
   static constexpr int BAR_BYTES = 512;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > FLCE_MAX_STAGES ? FLCE_MAX_STAGES : STAGES_FIT;
@@ -92,7 +110,6 @@ constexpr int TN_DLOGITS = FLCE_TN_DLOGITS;
 constexpr int TN_DWEIGHT = FLCE_TN_DWEIGHT;
 constexpr int TN_DHIDDEN = FLCE_TN_DHIDDEN;
 
-enum EpiKind { EPI_FWD_STATS = 0, EPI_DLOGITS = 1, EPI_STORE_BF16 = 2, EPI_ACCUM = 3 };
 enum AccMode { ACC_FIRST = 0, ACC_MID = 1, ACC_LAST = 2, ACC_ONLY = 3 };
 
 struct GemmShape {
@@ -538,11 +555,11 @@ struct Epilogue<EPI_ACCUM> {
 // tmem-full barriers of its own pair.  Each CTA's epilogue reads its own 128 TMEM
 // lanes (rows) and arrives on its pair leader's tmem-empty barrier.
 template <int EPI, bool A_MN, bool B_MN, int TN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
                           const EpiArgs ea) {
-  using C = PairCfg<TN>;
+  using C = PairCfg<TN, epi_warps<EPI>()>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -573,7 +590,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * NUM_EPI_WARPS);
+      mbar_init(&tempty[a], 2 * epi_warps<EPI>());
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -713,7 +730,7 @@ template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmShape& sh, const EpiArgs& ea, int max_clusters,
                              cudaStream_t stream) {
-  using C = PairCfg<TN>;
+  using C = PairCfg<TN, epi_warps<EPI>()>;
   auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN, TN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -729,7 +746,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(pair_threads<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -743,7 +760,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
 // current device.
 template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t pair_max_clusters(int csize, int* out) {
-  using C = PairCfg<TN>;
+  using C = PairCfg<TN, epi_warps<EPI>()>;
   auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN, TN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -755,7 +772,7 @@ cudaError_t pair_max_clusters(int csize, int* out) {
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(pair_threads<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
