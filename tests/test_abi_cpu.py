@@ -208,3 +208,41 @@ def test_selftest_wait_timeout_argument_checks(lib):
     assert lib.flce_selftest_wait_timeout(ok, 256, 0, None) == 1
     assert lib.flce_selftest_wait_timeout(ok, 256, 3_000_000_000, None) == 1
     assert lib.flce_selftest_wait_timeout(ok, 16, 1000, None) == 4
+
+
+def test_plain_c_program_links_and_calls_the_library(lib, tmp_path):
+    """The boundary is a C ABI: a C program (no Python, no torch) links libflce.so, sizes
+    a workspace and gets the documented host-side errors back (no GPU needed)."""
+    import subprocess
+    src = tmp_path / "use_flce.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "flce.h"
+int main(void) {
+  flce_params p;
+  memset(&p, 0, sizeof(p));
+  p.N = 8192; p.H = 4096; p.V = 128256; p.ignore_index = -100;
+  p.reduction = FLCE_RED_MEAN; p.zloss_coef = 1e-4f;
+  size_t ws0 = flce_workspace_size(&p, 0), ws1 = flce_workspace_size(&p, 1);
+  int bad_null = flce_forward(&p, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL);
+  p.H = 4100;  /* not a multiple of 8 */
+  int bad_align = flce_forward(&p, (void*)0x1000, (void*)0x1000, (void*)0x1000, (void*)0x1000,
+                               (void*)0x1000, (void*)0x1000, (void*)0x1000, (void*)0x1000,
+                               1 << 20, NULL);
+  printf("%d %zu %zu %d %d %s\n", flce_version(), ws0, ws1, bad_null, bad_align,
+         flce_strerror(FLCE_ERR_ALIGN));
+  return 0;
+}
+''')
+    exe = tmp_path / "use_flce"
+    libdir = os.path.dirname(B.LIB_PATH)
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir,
+                    "-l:libflce.so", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    p = flce.make_params(8192, 4096, 128256, "mean", zloss_coef=1e-4)
+    assert int(out[0]) == lib.flce_version()
+    assert int(out[1]) == flce.workspace_size(p, 0)
+    assert int(out[2]) == flce.workspace_size(p, 1)
+    assert int(out[3]) == 1 and int(out[4]) == 3
+    assert "aligned" in " ".join(out[5:])
