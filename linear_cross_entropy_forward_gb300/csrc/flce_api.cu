@@ -2,8 +2,8 @@
 // the launch sequence of the forward and backward passes (declared in flce.h).
 //
 // Forward  (verl PR #462, "Equivalent compute logic", without the [N,V] logits):
-//   1. fwd_stats GEMM: hidden @ weight tile by tile, each 128-column block of a
-//      row reduced to online-softmax partials (m, d, s) plus the label logit.
+//   1. fwd_stats GEMM: hidden @ weight tile by tile, each row's 256 columns of a
+//      tile reduced to online-softmax partials (m, d, s) plus the label logit.
 //   2. fwd_combine: merge the partials of a row -> lse, E_p[z], CE, entropy,
 //      z-loss, ignore mask (Liger-Kernel PR #551 / PR #435 semantics).
 //   3. reduce (mean/sum only): fixed-order fp64 sum over rows.
@@ -58,7 +58,7 @@ constexpr size_t kWsumOffset = 64;  // float in the workspace header: sum of cla
 
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
-  L.n_parts = PairCfg<TN_FWD, epi_warps<EPI_FWD_STATS>()>::PARTS * cdiv(p->V, TN_FWD);  // one part per warp's columns
+  L.n_parts = PairCfg<TN_FWD, epi_warps<EPI_FWD_STATS>()>::PARTS * cdiv(p->V, TN_FWD);  // parts per tile x tiles
   const size_t part_bytes = align256(static_cast<size_t>(L.n_parts * p->N) * 4);
   const size_t row_bytes = align256(static_cast<size_t>(p->N) * 4);
   size_t off = kHeaderBytes;
