@@ -350,4 +350,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 256-bit global accesses (one full 32-byte sector per thread; sm_100 and later).
+// The address must be 32-byte aligned: callers use them only on workspace arrays
+// whose base is 256-byte aligned and whose row pitch and offsets are multiples of
+// 32 bytes.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                  "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Evict-first variant, for data that the next kernel streams once.
+__device__ __forceinline__ void st_global_cs_v8f(float* p, const float* v) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+                  "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global_v8f(float* p, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+                  "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_global_v8f(const float* p, float* v) {
+  asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p)
+               : "memory");
+}
+
 }  // namespace flce

@@ -272,10 +272,9 @@ struct Epilogue<EPI_FWD_STATS> {
       const int vb = vcol0 + ch * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
       if (zrow) {
-        float4* z4 = reinterpret_cast<float4*>(zrow + ch * 32);
+        // 32-byte aligned: 256-aligned workspace, pitch a multiple of 256 floats
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          z4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) st_global_cs_v8f(zrow + ch * 32 + q * 8, x + q * 8);
       }
       // the label's logit (natural units), from the one chunk that holds it
       if (static_cast<unsigned>(y - vb) < 32u) {
@@ -469,10 +468,9 @@ struct Epilogue<EPI_DLOGITS> {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        // 32-byte aligned: 256-aligned workspace, chunk pitch a multiple of 256 columns
+        st_global_v8(dst + ch * 32, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+        st_global_v8(dst + ch * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8));
       }
     }
   }
@@ -523,19 +521,20 @@ struct Epilogue<EPI_ACCUM> {
       for (int q = 0; q < 4; ++q) {
         const int col = col0 + c * 32 + q * 8;
         if (col >= ea.cols) continue;
+        // the fp32 accumulator lives in the workspace (256-aligned, pitch a multiple
+        // of 8 floats): 32-byte aligned
         float* a = ea.acc + base + c * 32 + q * 8;
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = x[q * 8 + i];
         if (ea.acc_mode == ACC_MID || ea.acc_mode == ACC_LAST) {
-          const float4 o0 = reinterpret_cast<const float4*>(a)[0];
-          const float4 o1 = reinterpret_cast<const float4*>(a)[1];
-          v[0] += o0.x; v[1] += o0.y; v[2] += o0.z; v[3] += o0.w;
-          v[4] += o1.x; v[5] += o1.y; v[6] += o1.z; v[7] += o1.w;
+          float o[8];
+          ld_global_v8f(a, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] += o[i];
         }
         if (ea.acc_mode == ACC_FIRST || ea.acc_mode == ACC_MID) {
-          reinterpret_cast<float4*>(a)[0] = make_float4(v[0], v[1], v[2], v[3]);
-          reinterpret_cast<float4*>(a)[1] = make_float4(v[4], v[5], v[6], v[7]);
+          st_global_v8f(a, v);
         } else {
           uint4 o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
