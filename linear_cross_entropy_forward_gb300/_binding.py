@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG_DIR, "libflce.so")
 
 FLCE_OK = 0
 _ERR_NAMES = {1: "BAD_ARG", 2: "BAD_SHAPE", 3: "ALIGN", 4: "WS_TOO_SMALL", 5: "LABEL",
-              6: "TIMEOUT", 7: "CUDA", 8: "DEVICE"}
+              6: "TIMEOUT", 7: "CUDA", 8: "DEVICE", 9: "SCRATCH_LIMIT"}
 
 
 class FlceError(RuntimeError):

@@ -36,9 +36,18 @@ def test_header_declares_the_exported_set(lib):
 
 def test_version_and_strerror(lib):
     assert lib.flce_version() == 200
-    for code in range(0, 9):
+    for code in range(0, 10):
         assert lib.flce_strerror(code)
+        assert b"unknown" not in lib.flce_strerror(code)
     assert b"unknown" in lib.flce_strerror(99)
+
+
+def test_error_codes_match_the_header():
+    """Every FLCE_ERR_* code of the header has its name in the binding's error messages."""
+    codes = dict((name, int(v)) for name, v in
+                 re.findall(r"FLCE_ERR_([A-Z_]+)\s*=\s*(\d+)", open(HEADER).read()))
+    assert codes and max(codes.values()) == 9
+    assert {v: k for k, v in codes.items()} == B._ERR_NAMES
 
 
 def test_params_struct_layout():
