@@ -146,7 +146,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _need(t, name, dtype, shape):
+def _need(t, name, dtype, shape, device=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
@@ -155,6 +155,24 @@ def _need(t, name, dtype, shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the other tensors on {device}")
+
+
+def _on_current_device(t):
+    """The library launches on the current CUDA device: the tensors must live there."""
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {t.device} but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
+    return t.device
+
+
+def _need_out(out, names_shapes_dtypes, device):
+    if len(out) != len(names_shapes_dtypes):
+        raise ValueError(f"out must hold {len(names_shapes_dtypes)} tensors")
+    for t, (name, shape, dtype) in zip(out, names_shapes_dtypes):
+        _need(t, name, dtype, shape, device)
+    return out
 
 
 def _stream(stream):
@@ -164,6 +182,10 @@ def _stream(stream):
 
 def _workspace(params, phase, device, workspace):
     need = workspace_size(params, phase)
+    if workspace is not None:
+        if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 \
+                or not workspace.is_contiguous() or workspace.device != device:
+            raise TypeError(f"workspace must be a contiguous uint8 tensor on {device}")
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     return workspace
@@ -182,14 +204,14 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, wshape)
-    _need(labels, "labels", torch.int64, (N,))
+    dev = _on_current_device(hidden)
+    _need(weight, "weight", torch.bfloat16, wshape, dev)
+    _need(labels, "labels", torch.int64, (N,), dev)
     if class_weight is not None:
-        _need(class_weight, "class_weight", torch.float32, (V,))
+        _need(class_weight, "class_weight", torch.float32, (V,), dev)
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
                     weight_layout=weight_layout, label_smoothing=label_smoothing,
                     class_weight=class_weight)
-    dev = hidden.device
     n_out = N if p.reduction == RED_NONE else 1
     if out is None:
         loss = torch.empty(n_out, dtype=torch.float32, device=dev)
@@ -197,7 +219,9 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
         lse = torch.empty(N, dtype=torch.float32, device=dev)
         ez = torch.empty(N, dtype=torch.float32, device=dev)
     else:
-        loss, ent, lse, ez = out
+        f32 = torch.float32
+        loss, ent, lse, ez = _need_out(out, [("loss", (n_out,), f32), ("entropy", (n_out,), f32),
+                                             ("lse", (N,), f32), ("ez", (N,), f32)], dev)
     ws = _workspace(p, 0, dev, workspace)
     _check(lib.flce_forward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                             _ptr(loss), _ptr(ent), _ptr(lse), _ptr(ez), _ptr(ws), ws.numel(),
@@ -219,25 +243,26 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, wshape)
-    _need(labels, "labels", torch.int64, (N,))
-    _need(lse, "lse", torch.float32, (N,))
-    _need(ez, "ez", torch.float32, (N,))
+    dev = _on_current_device(hidden)
+    _need(weight, "weight", torch.bfloat16, wshape, dev)
+    _need(labels, "labels", torch.int64, (N,), dev)
+    _need(lse, "lse", torch.float32, (N,), dev)
+    _need(ez, "ez", torch.float32, (N,), dev)
     if class_weight is not None:
-        _need(class_weight, "class_weight", torch.float32, (V,))
+        _need(class_weight, "class_weight", torch.float32, (V,), dev)
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v,
                     weight_layout, label_smoothing, class_weight, v_offset, v_total)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
-        _need(g_loss, "g_loss", torch.float32, (n_g,))
+        _need(g_loss, "g_loss", torch.float32, (n_g,), dev)
     if g_entropy is not None:
-        _need(g_entropy, "g_entropy", torch.float32, (n_g,))
-    dev = hidden.device
+        _need(g_entropy, "g_entropy", torch.float32, (n_g,), dev)
     if out is None:
         dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
         dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
     else:
-        dh, dw = out
+        bf = torch.bfloat16
+        dh, dw = _need_out(out, [("dhidden", (N, H), bf), ("dweight", wshape, bf)], dev)
     ws = _workspace(p, 1, dev, workspace)
     _check(lib.flce_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                              _ptr(lse), _ptr(ez), _ptr(g_loss), _ptr(g_entropy), _ptr(dh),
@@ -258,19 +283,19 @@ def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, wshape)
-    _need(labels, "labels", torch.int64, (N,))
+    dev = _on_current_device(hidden)
+    _need(weight, "weight", torch.bfloat16, wshape, dev)
+    _need(labels, "labels", torch.int64, (N,), dev)
     if class_weight is not None:
-        _need(class_weight, "class_weight", torch.float32, (V,))
+        _need(class_weight, "class_weight", torch.float32, (V,), dev)
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
                     weight_layout=weight_layout, label_smoothing=label_smoothing,
                     class_weight=class_weight, chunk_n=chunk_n)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
-        _need(g_loss, "g_loss", torch.float32, (n_g,))
+        _need(g_loss, "g_loss", torch.float32, (n_g,), dev)
     if g_entropy is not None:
-        _need(g_entropy, "g_entropy", torch.float32, (n_g,))
-    dev = hidden.device
+        _need(g_entropy, "g_entropy", torch.float32, (n_g,), dev)
     if out is None:
         loss = torch.empty(n_g, dtype=torch.float32, device=dev)
         ent = torch.empty(n_g, dtype=torch.float32, device=dev)
@@ -279,7 +304,10 @@ def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="
         dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
         dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
     else:
-        loss, ent, lse, ez, dh, dw = out
+        f32, bf = torch.float32, torch.bfloat16
+        loss, ent, lse, ez, dh, dw = _need_out(
+            out, [("loss", (n_g,), f32), ("entropy", (n_g,), f32), ("lse", (N,), f32),
+                  ("ez", (N,), f32), ("dhidden", (N, H), bf), ("dweight", wshape, bf)], dev)
     ws = _workspace(p, 3, dev, workspace)
     _check(lib.flce_forward_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                                      _ptr(g_loss), _ptr(g_entropy), _ptr(loss), _ptr(ent),
@@ -294,7 +322,8 @@ def flce_scale_bf16(x, g, stream=None):
     if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.bfloat16 \
             or not x.is_contiguous():
         raise TypeError("x must be a contiguous CUDA bf16 tensor")
-    _need(g, "g", torch.float32, (1,))
+    dev = _on_current_device(x)
+    _need(g, "g", torch.float32, (1,), dev)
     _check(load_library().flce_scale_bf16(_ptr(x), x.numel(), _ptr(g), _stream(stream)))
     return x
 
@@ -307,13 +336,15 @@ def flce_shard_stats(hidden, weight, labels, v_offset, v_total, softcap=0.0,
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
     _need(hidden, "hidden", torch.bfloat16, (N, H))
-    _need(weight, "weight", torch.bfloat16, wshape)
-    _need(labels, "labels", torch.int64, (N,))
+    dev = _on_current_device(hidden)
+    _need(weight, "weight", torch.bfloat16, wshape, dev)
+    _need(labels, "labels", torch.int64, (N,), dev)
     p = make_params(N, H, V, "none", ignore_index, 0.0, softcap, validate,
                     weight_layout=weight_layout, v_offset=v_offset, v_total=v_total)
-    stats = out if out is not None else torch.empty(4, N, dtype=torch.float32,
-                                                    device=hidden.device)
-    ws = _workspace(p, 0, hidden.device, workspace)
+    if out is not None:
+        _need(out, "out", torch.float32, (4, N), dev)
+    stats = out if out is not None else torch.empty(4, N, dtype=torch.float32, device=dev)
+    ws = _workspace(p, 0, dev, workspace)
     _check(lib.flce_shard_stats(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                                 _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)))
     return stats
@@ -326,10 +357,10 @@ def flce_combine_shards(stats, labels, v_total, reduction="mean", ignore_index=I
     lib = load_library()
     P, four, N = stats.shape
     _need(stats, "stats", torch.float32, (P, 4, N))
-    _need(labels, "labels", torch.int64, (N,))
+    dev = _on_current_device(stats)
+    _need(labels, "labels", torch.int64, (N,), dev)
     p = make_params(N, H, v_total, reduction, ignore_index, zloss_coef, 0.0, validate,
                     v_offset=0, v_total=v_total)
-    dev = stats.device
     n_out = N if p.reduction == RED_NONE else 1
     loss = torch.empty(n_out, dtype=torch.float32, device=dev)
     ent = torch.empty(n_out, dtype=torch.float32, device=dev)

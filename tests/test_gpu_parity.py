@@ -255,3 +255,35 @@ def test_autograd_function_matches_explicit_calls():
     dh, dw = flce_backward(h.detach(), W.detach(), y, lse, ez, torch.ones(1, device=dev),
                            torch.full((1,), 0.5, device=dev), "mean")
     assert torch.equal(h.grad, dh) and torch.equal(W.grad, dw)
+
+
+def test_binding_rejects_mismatched_outputs_and_workspace():
+    """Caller-provided outputs and workspaces are checked on the host before any launch."""
+    _cuda_or_skip()
+    from linear_cross_entropy_forward_gb300 import flce_forward_backward
+    dev = torch.device("cuda")
+    hidden = torch.randn(64, 64, device=dev).to(torch.bfloat16)
+    weight = torch.randn(64, 256, device=dev).to(torch.bfloat16)
+    labels = torch.zeros(64, dtype=torch.int64, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    good = (torch.empty(64, **f32), torch.empty(64, **f32), torch.empty(64, **f32),
+            torch.empty(64, **f32))
+    flce_forward(hidden, weight, labels, "none", out=good)
+    with pytest.raises(ValueError):  # wrong shape
+        flce_forward(hidden, weight, labels, "none", out=(good[0][:32],) + good[1:])
+    with pytest.raises(TypeError):  # wrong dtype
+        flce_forward(hidden, weight, labels, "none",
+                     out=(good[0].double(),) + good[1:])
+    with pytest.raises(ValueError):  # too few tensors
+        flce_forward(hidden, weight, labels, "none", out=good[:3])
+    with pytest.raises(TypeError):  # workspace not bytes
+        flce_forward(hidden, weight, labels, "none", workspace=torch.empty(1 << 20, **f32))
+    dh = torch.empty(64, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError):  # dweight shaped like dhidden
+        flce_backward(hidden, weight, labels, good[2], good[3], None, None, "none",
+                      out=(dh, torch.empty(64, 64, dtype=torch.bfloat16, device=dev)))
+    with pytest.raises(ValueError):
+        flce_forward_backward(hidden, weight, labels, None, None, "mean",
+                              out=(torch.empty(64, **f32),) * 4 + (dh, dh))
+    with pytest.raises(TypeError):  # a CPU tensor among CUDA ones
+        flce_forward(hidden, weight, labels.cpu(), "none")
