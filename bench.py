@@ -66,6 +66,16 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def blas_threads() -> int:
+    """Threads the oracle's BLAS runs on: the OpenBLAS / OpenMP thread variables when
+    set (read when numpy loads), else every host core."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return min(int(v), host_cores())
+    return host_cores()
+
+
 L2_BYTES = 129 * 10**6     # GB300 L2
 FLUSH_BYTES = 512 << 20     # written between timed steps when the inputs fit in L2
 
@@ -133,9 +143,9 @@ def cpu_baseline(w, hidden, weight, labels, g_loss, g_ent, seconds):
     t0 = time.perf_counter()
     oracle_sample_step(w, *ai, rows=rows)
     dt = time.perf_counter() - t0
-    return {"value": rows / dt, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+    return {"value": rows / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"fp64 numpy oracle fwd+bwd on the first {rows} of {w.N} rows "
-                      f"(full H={w.H}, V={w.V}), {dt:.1f} s; BLAS threads = host cores"}
+                      f"(full H={w.H}, V={w.V}), {dt:.1f} s on {blas_threads()} BLAS threads"}
 
 
 # ---------------------------------------------------------------- clocks sampler
@@ -534,7 +544,7 @@ def run_reference(args):
            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": workload_config(w, 1),
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
@@ -544,6 +554,12 @@ def run_reference(args):
 def main():
     args = parse_args()
     if args.impl == "reference":
+        rank, world, _ = dist_env()
+        if world > 1 and rank == 0:
+            # torchrun sets one OpenMP thread per rank; here the other ranks do no work,
+            # so rank 0's oracle gets every core (numpy is not loaded yet)
+            os.environ["OPENBLAS_NUM_THREADS"] = os.environ["OMP_NUM_THREADS"] = \
+                str(host_cores())
         run_reference(args)
     else:
         run_ours(args)
