@@ -46,7 +46,8 @@
  *     that timed out) are recorded in an error word inside the workspace; they
  *     are returned by flce_status(), or directly when params->validate != 0.
  *   - Requirements: N >= 0, H >= 8, V >= 1, H % 8 == 0, V % 8 == 0 (16-byte row
- *     strides for the TMA engine); every pointer 16-byte aligned.
+ *     strides for the TMA engine); every tensor pointer 16-byte aligned (g_loss,
+ *     g_entropy and class_weight: 4-byte), every workspace 256-byte aligned.
  */
 #ifndef FLCE_H_
 #define FLCE_H_
