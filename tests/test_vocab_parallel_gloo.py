@@ -69,3 +69,41 @@ def test_two_rank_vocab_parallel_exchange(reduction, cap):
 
 def test_three_rank_vocab_parallel_exchange():
     mp.spawn(_worker, args=(3, _free_port(), "mean", 1.5), nprocs=3, join=True)
+
+
+def _worker_peer_leaves(rank, world, port, flag_path):
+    """Rank 1 leaves before the exchange (between steps, nothing in flight); rank 0's
+    exchange must end with an error within the process group's timeout, not hang."""
+    import datetime
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from linear_cross_entropy_forward_gb300.vocab_parallel import exchange_stats
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world, timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        os._exit(0)  # the rank is gone: no destroy, no further collective
+    try:
+        exchange_stats(torch.zeros(4, 8, dtype=torch.float64))
+    except Exception as e:  # gloo reports the lost peer (or the timeout) as an error
+        with open(flag_path, "w") as f:
+            f.write(type(e).__name__)
+    finally:
+        os._exit(0)
+
+
+def test_exchange_reports_a_rank_that_left(tmp_path):
+    flag = tmp_path / "detected"
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_peer_leaves, args=(r, 2, port, str(flag)))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=60)
+    alive = [p for p in procs if p.is_alive()]
+    for p in alive:
+        p.kill()
+    assert not alive, "a rank hung instead of reporting the lost peer"
+    assert flag.exists(), "rank 0's exchange did not raise"
