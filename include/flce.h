@@ -208,6 +208,23 @@ int flce_kernel_launches(const flce_params* params, int phase);
  * FLCE_OK once the kernel is enqueued (the timeout is the expected outcome). */
 int flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns, void* stream);
 
+/* Diagnostic (no counterpart on the pages): the schedule the library plans for one of
+ * its GEMMs, from the GEMM's shape in tiles and the GPU's capacity; host arithmetic
+ * only, usable without a GPU.
+ *   m_tiles, n_tiles: output tiles (256 rows x tn columns); raster: 0 = the M tiles
+ *   vary fastest in the persistent schedule, 1 = the N tiles; panel_bytes: bytes of the
+ *   operand every tile of a raster group revisits, per tile of the fast dimension;
+ *   a_hint, b_hint: the L2 policy wanted for the A / B loads (0 normal, 1 evict-first,
+ *   2 evict-last); clusters4, clusters2: clusters of four CTAs and CTA pairs the GPU
+ *   holds at once (36 and 76 on a 152-SM GB300).
+ *   out[4] receives: operand sharing (0 none, 1 two pairs along M share B, 2 two pairs
+ *   along N share A), tiles of the fast dimension per raster group (in cluster tiles),
+ *   and the L2 policies of the A and B loads.
+ * Returns FLCE_OK, or FLCE_ERR_BAD_ARG for a NULL out or an out-of-range argument. */
+int flce_plan_tiles(int32_t m_tiles, int32_t n_tiles, int32_t raster, int64_t panel_bytes,
+                    int32_t tn, int32_t a_hint, int32_t b_hint, int32_t clusters4,
+                    int32_t clusters2, int32_t* out);
+
 /* Static, NUL-terminated description of a status code. */
 const char* flce_strerror(int code);
 

@@ -57,7 +57,7 @@ _lock = threading.Lock()
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
             "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc",
             "flce_shard_stats", "flce_combine_shards", "flce_forward_backward",
-            "flce_scale_bf16", "flce_selftest_wait_timeout")
+            "flce_scale_bf16", "flce_selftest_wait_timeout", "flce_plan_tiles")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -97,6 +97,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flce_scale_bf16.restype = ctypes.c_int
         lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint64, vp]
         lib.flce_selftest_wait_timeout.restype = ctypes.c_int
+        i32 = ctypes.c_int32
+        lib.flce_plan_tiles.argtypes = [i32, i32, i32, ctypes.c_int64, i32, i32, i32, i32, i32,
+                                        ctypes.POINTER(i32)]
+        lib.flce_plan_tiles.restype = ctypes.c_int
         lib.flce_version.argtypes = []
         lib.flce_version.restype = ctypes.c_int
         _lib = lib
@@ -135,6 +139,16 @@ def workspace_size(params: FlceParams, phase: int) -> int:
     if n == 0:
         raise FlceError(1, "invalid parameters for workspace sizing")
     return int(n)
+
+
+def plan_tiles(m_tiles, n_tiles, raster, panel_bytes, tn=256, a_hint=0, b_hint=0,
+               clusters4=36, clusters2=76):
+    """The GEMM schedule the library plans (host arithmetic, no GPU needed):
+    (share, group, a_hint, b_hint); see flce_plan_tiles in flce.h."""
+    out = (ctypes.c_int32 * 4)()
+    _check(load_library().flce_plan_tiles(m_tiles, n_tiles, raster, panel_bytes, tn, a_hint,
+                                          b_hint, clusters4, clusters2, out))
+    return tuple(out)
 
 
 def kernel_launches(params: FlceParams, phase: int) -> int:

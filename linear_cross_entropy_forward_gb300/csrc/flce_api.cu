@@ -287,7 +287,9 @@ int raster_group(int64_t panel_bytes, int fast_tiles) {
 #ifndef FLCE_CLUSTER_SHARE
 #define FLCE_CLUSTER_SHARE 2
 #endif
-void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
+// The plan from the tile counts and the numbers of clusters of four (c4) and of CTA
+// pairs (c2) the GPU holds at once: host arithmetic only.
+void plan_tiles_for(GemmShape* sh, int64_t panel_bytes, int tn, int64_t c4, int64_t c2) {
   int share = 0;
   if (FLCE_CLUSTER_SHARE && tn == 256) {
     if (sh->m_tiles % 2 == 0)
@@ -298,7 +300,6 @@ void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
       share = sh->m_tiles >= sh->n_tiles ? 1 : 2;
   }
   if (share && FLCE_CLUSTER_SHARE == 2) {
-    const int64_t c4 = cluster_capacity(4), c2 = cluster_capacity(2);
     const int64_t pair_tiles = int64_t(sh->m_tiles) * sh->n_tiles;
     const int64_t quad_tiles = (share == 1 ? cdiv(sh->m_tiles, 2) * sh->n_tiles
                                            : sh->m_tiles * cdiv(sh->n_tiles, 2));
@@ -315,7 +316,7 @@ void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
   // When few panels fit the L2 budget, a square-ish set of resident tiles reads
   // fewer distinct rows and columns: the k-steps of all resident tiles advance
   // together (persistent schedule), so only the k-slices in flight need to be in L2.
-  const int64_t cap = cluster_capacity(share ? 4 : 2);
+  const int64_t cap = share ? c4 : c2;
   int g = 1;
   while (int64_t(g + 1) * (g + 1) <= cap) ++g;
   const int budget_group = raster_group(panel, fast);
@@ -328,6 +329,10 @@ void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
   } else {
     sh->group = budget_group;
   }
+}
+
+void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
+  plan_tiles_for(sh, panel_bytes, tn, cluster_capacity(4), cluster_capacity(2));
 }
 
 GemmShape base_shape(int a_hint, int b_hint) {
@@ -398,6 +403,25 @@ int flce_kernel_launches(const flce_params* p, int phase) {
 int flce_status(const void* workspace, void* stream) {
   if (!workspace) return FLCE_ERR_BAD_ARG;
   return read_status(workspace, static_cast<cudaStream_t>(stream));
+}
+
+int flce_plan_tiles(int32_t m_tiles, int32_t n_tiles, int32_t raster, int64_t panel_bytes,
+                    int32_t tn, int32_t a_hint, int32_t b_hint, int32_t clusters4,
+                    int32_t clusters2, int32_t* out) {
+  if (!out || m_tiles < 1 || n_tiles < 1 || (raster != 0 && raster != 1) || panel_bytes < 0 ||
+      tn < 1 || a_hint < 0 || a_hint > 2 || b_hint < 0 || b_hint > 2 || clusters4 < 0 ||
+      clusters2 < 1)
+    return FLCE_ERR_BAD_ARG;
+  GemmShape sh = base_shape(a_hint, b_hint);
+  sh.m_tiles = m_tiles;
+  sh.n_tiles = n_tiles;
+  sh.raster = raster;
+  plan_tiles_for(&sh, panel_bytes, tn, clusters4, clusters2);
+  out[0] = sh.share;
+  out[1] = sh.group;
+  out[2] = sh.a_hint;
+  out[3] = sh.b_hint;
+  return FLCE_OK;
 }
 
 }  // extern "C"
