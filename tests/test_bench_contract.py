@@ -56,3 +56,16 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     sys.path.insert(0, ROOT)
     import bench
     assert d["cpu_baseline"]["cores"] == bench.host_cores()
+
+
+def test_peak_comes_from_the_measured_file_when_present(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.load_peaks(str(tmp_path)) == (1900.0, "of fallback (1.9 PFLOP/s bf16 burst)")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 7100.0, "bf16_tflops": 2050.0, "bf16_tflops_sustained": 1720.0}))
+    assert bench.load_peaks(str(tmp_path)) == (1720.0, "of measured (bf16_tflops_sustained)")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": {"value": 2010.0}}))
+    assert bench.load_peaks(str(tmp_path)) == (2010.0, "of measured (bf16_tflops)")
+    (tmp_path / "MEASURED_PEAKS.json").write_text("not json")
+    assert bench.load_peaks(str(tmp_path))[0] == 1900.0
