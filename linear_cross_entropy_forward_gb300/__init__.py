@@ -11,7 +11,8 @@ keeps one token chunk's logits instead and skips the backward's recompute.
 from ._binding import (FlceError, FlceParams, flce_backward, flce_combine_shards,  # noqa: F401
                        flce_forward, flce_forward_backward, flce_scale_bf16,
                        flce_shard_stats, flce_status, kernel_launches,
-                       linear_cross_entropy, load_library, make_params, workspace_size,
+                       linear_cross_entropy, load_library, make_params, plan_tiles,
+                       selftest_wait_timeout, workspace_size,
                        LIB_PATH, EXPORTED)
 from .pipeline import HostPipeline  # noqa: F401
 from .vocab_parallel import (exchange_stats, reduce_dhidden,  # noqa: F401
