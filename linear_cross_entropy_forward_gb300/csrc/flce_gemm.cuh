@@ -23,6 +23,9 @@
 //     EPI_STORE_BF16 plain bf16 store (dweight tiles).
 //     EPI_ACCUM      fp32 accumulation across vocabulary chunks (dhidden) or token
 //                    chunks (dweight); the last chunk writes bf16.
+//   Arrays in the workspace (kept logits, dlogits, fp32 accumulators: 256-byte
+//   aligned, pitches multiples of 32 bytes) are accessed 256 bits per thread; the
+//   caller's dweight / dhidden (16-byte alignment promised) 128 bits.
 //
 // A cluster holds one pair, or two pairs whose tiles lie side by side along M
 // (then they read the same B columns) or along N (the same A rows).  The shared
