@@ -1,5 +1,5 @@
 """bench.py's output contract, checked on the CPU through its reference arm (the fp64
-oracle timed on the host): one JSON line with the keys and types the driver reads."""
+oracle timed on the host): one JSON line with the keys and types its readers rely on."""
 import json
 import os
 import subprocess
