@@ -167,10 +167,10 @@ struct EpiArgs {
 
 // Cluster tiles: with two pairs per cluster, a cluster tile is two pair tiles
 // along the shared dimension.
-__device__ __forceinline__ int cluster_m_tiles(const GemmShape& sh) {
+__host__ __device__ __forceinline__ int cluster_m_tiles(const GemmShape& sh) {
   return sh.share == 1 ? (sh.m_tiles + 1) >> 1 : sh.m_tiles;
 }
-__device__ __forceinline__ int cluster_n_tiles(const GemmShape& sh) {
+__host__ __device__ __forceinline__ int cluster_n_tiles(const GemmShape& sh) {
   return sh.share == 2 ? (sh.n_tiles + 1) >> 1 : sh.n_tiles;
 }
 
@@ -179,9 +179,10 @@ __device__ __forceinline__ int cluster_n_tiles(const GemmShape& sh) {
 // m-tile count: plain m-fastest order).  raster 1: the same with the roles of m and
 // n swapped.  Grouping bounds how much of the operand revisited by every tile must
 // stay in L2.  The pair's own tile is then picked inside the cluster tile; it can
-// lie past the last tile when the shared dimension has an odd tile count.
-__device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int pair, int& mt,
-                                            int& nt) {
+// lie past the last tile when the shared dimension has an odd tile count.  (Host
+// callable too, so the order can be checked without a GPU.)
+__host__ __device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int pair,
+                                                     int& mt, int& nt) {
   const int cm = cluster_m_tiles(sh), cn = cluster_n_tiles(sh);
   const bool m_major = sh.raster == 0;
   const int fast_tiles = m_major ? cm : cn;

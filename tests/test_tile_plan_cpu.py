@@ -73,3 +73,84 @@ def test_plan_rejects_bad_arguments(bad):
     with pytest.raises(B.FlceError) as ei:
         B.plan_tiles(a["m"], a["n"], a["raster"], MiB, 256, a["ah"], 0, 36, a["c2"])
     assert ei.value.code == 1
+
+
+TILE_ORDER_CHECK = r"""
+#include <cstdio>
+#include <vector>
+#include "flce_gemm.cuh"
+using namespace flce;
+
+// Every output tile is visited exactly once over all cluster tiles and pairs; a tile
+// past the end appears only for the spare half of a cluster tile along an odd shared
+// dimension.
+static int check(int m, int n, int share, int raster, int group) {
+  GemmShape sh{};
+  sh.m_tiles = m; sh.n_tiles = n; sh.share = share; sh.raster = raster; sh.group = group;
+  const int total = cluster_m_tiles(sh) * cluster_n_tiles(sh);
+  const int pairs = share ? 2 : 1;
+  std::vector<int> hits(static_cast<size_t>(m) * n, 0);
+  int spare = 0;
+  for (int t = 0; t < total; ++t)
+    for (int p = 0; p < pairs; ++p) {
+      int mt, nt;
+      tile_coords(t, sh, p, mt, nt);
+      if (mt < 0 || nt < 0) return 1;
+      if (mt >= m || nt >= n) {
+        const bool ok = (share == 1 && (m & 1) && mt == m && nt < n) ||
+                        (share == 2 && (n & 1) && nt == n && mt < m);
+        if (!ok) return 2;
+        ++spare;
+        continue;
+      }
+      ++hits[static_cast<size_t>(mt) * n + nt];
+    }
+  for (int h : hits)
+    if (h != 1) return 3;
+  const int want_spare = share == 1 ? (m & 1) * n : share == 2 ? (n & 1) * m : 0;
+  return spare == want_spare ? 0 : 4;
+}
+
+int main() {
+  const int dims[] = {1, 2, 3, 5, 8, 13, 16, 32, 37};
+  const int groups[] = {1, 2, 3, 6, 8, 10, 1 << 30};
+  long cases = 0;
+  for (int m : dims)
+    for (int n : dims)
+      for (int share = 0; share < 3; ++share)
+        for (int raster = 0; raster < 2; ++raster)
+          for (int g : groups) {
+            const int rc = check(m, n, share, raster, g);
+            if (rc) {
+              std::printf("FAIL %d m=%d n=%d share=%d raster=%d group=%d\n", rc, m, n, share,
+                          raster, g);
+              return 1;
+            }
+            ++cases;
+          }
+  std::printf("OK %ld\n", cases);
+  return 0;
+}
+"""
+
+
+def test_tile_order_covers_every_tile_once(tmp_path):
+    """The persistent schedule's tile order (tile_coords, compiled for the host with
+    nvcc): every output tile exactly once for every share, raster and group choice,
+    including ragged groups and odd shared dimensions."""
+    import os
+    import subprocess
+    from linear_cross_entropy_forward_gb300.build import CSRC, ROOT, nvcc_path
+    try:
+        nvcc = nvcc_path()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    src = tmp_path / "tile_order_check.cu"
+    src.write_text(TILE_ORDER_CHECK)
+    exe = tmp_path / "tile_order_check"
+    r = subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                        "-I" + CSRC, "-I" + os.path.join(ROOT, "include"), str(src), "-o",
+                        str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
