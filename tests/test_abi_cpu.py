@@ -255,3 +255,23 @@ int main(void) {
     assert int(out[2]) == flce.workspace_size(p, 1)
     assert int(out[3]) == 1 and int(out[4]) == 3
     assert "aligned" in " ".join(out[5:])
+
+
+def test_auto_chunking_follows_the_documented_rules(lib):
+    """flce.h: the backward's chunk_v = 0 picks the widest multiple of 256 columns whose bf16
+    dlogits [N, chunk_v] fit 1 GiB; flce_forward_backward's chunk_n = 0 the largest multiple
+    of 512 rows whose fp32 logits and bf16 dlogits (V rounded up to 256) fit 8 GiB.  Checked
+    through the launch counts (3 GEMMs per vocabulary chunk, 6 launches per token chunk)."""
+    import random
+    rng = random.Random(5)
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+    for _ in range(200):
+        N = rng.choice([1, 7, 300, 4096, 8192, 16384, 65536, 200000])
+        V = 8 * rng.randint(1, 40000)
+        vc = max(256, min((1 << 30) // (2 * N) // 256 * 256, cdiv(V, 256) * 256))
+        p = flce.make_params(N, 64, V, "none")
+        assert flce.kernel_launches(p, 1) == 1 + 3 * cdiv(V, vc), (N, V)
+        ldz = cdiv(V, 256) * 256
+        nc = max(512, (8 << 30) // (ldz * 6) // 512 * 512)
+        nc = min(nc, cdiv(N, 256) * 256)
+        assert flce.kernel_launches(p, 4) == 6 * cdiv(N, nc), (N, V)
