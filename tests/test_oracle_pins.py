@@ -68,6 +68,15 @@ def test_worked_examples(case):
     if "loss" in case:
         np.testing.assert_allclose(out["loss_tok"], [_ev(x) for x in case["loss"]], rtol=0,
                                    atol=1e-13)
+    if "backward" in case:
+        b = case["backward"]
+        dh, dw = orc.backward(hidden, weight, labels, out["lse"], out["ez"],
+                              np.array(b["g_loss"]), np.array(b["g_entropy"]), "none",
+                              zloss_coef=case["zloss_coef"], softcap=case["softcap"])
+        np.testing.assert_allclose(dw, [[_ev(x) for x in r] for r in b["dweight"]], rtol=0,
+                                   atol=1e-13)
+        np.testing.assert_allclose(dh, [[_ev(x) for x in r] for r in b["dhidden"]], rtol=0,
+                                   atol=1e-13)
 
 
 # --------------------------------------------------------------------------- closed forms
