@@ -210,6 +210,27 @@ def test_product_path_fails_loudly_without_library(tmp_path):
         B._lib = saved
 
 
+def test_cpu_tensors_are_refused_not_computed():
+    """There is no CPU fallback: host tensors are refused before anything runs."""
+    import torch
+    h = torch.zeros(16, 64, dtype=torch.bfloat16)
+    w = torch.zeros(64, 128, dtype=torch.bfloat16)
+    y = torch.zeros(16, dtype=torch.int64)
+    g = torch.ones(1)
+    calls = [
+        lambda: flce.flce_forward(h, w, y, "mean"),
+        lambda: flce.flce_backward(h, w, y, torch.zeros(16), torch.zeros(16), g, g, "mean"),
+        lambda: flce.flce_forward_backward(h, w, y, g, g, "mean"),
+        lambda: flce.linear_cross_entropy(h, w, y, "mean"),
+        lambda: flce.linear_cross_entropy(h, w, y, "mean", grad_in_forward=True),
+        lambda: flce.flce_shard_stats(h, w, y, 0, 128),
+        lambda: flce.flce_scale_bf16(h, g),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError, match="CUDA"):
+            call()
+
+
 def test_selftest_wait_timeout_argument_checks(lib):
     ok = ctypes.c_void_p(0x10000)
     assert lib.flce_selftest_wait_timeout(None, 256, 1000, None) == 1
