@@ -107,3 +107,30 @@ def test_exchange_reports_a_rank_that_left(tmp_path):
         p.kill()
     assert not alive, "a rank hung instead of reporting the lost peer"
     assert flag.exists(), "rank 0's exchange did not raise"
+
+
+def _worker_bf16_sum(rank, world, port, path):
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from linear_cross_entropy_forward_gb300.vocab_parallel import reduce_dhidden
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        g = torch.Generator().manual_seed(100 + rank)
+        part = torch.randn(33, 17, generator=g).to(torch.bfloat16)
+        out = reduce_dhidden(part)
+        assert out.dtype == torch.bfloat16 and out.shape == part.shape
+        torch.save((part, out), f"{path}.{rank}")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_dhidden_sums_bf16_terms_in_fp32(tmp_path):
+    """dhidden terms arrive in bf16; they are summed in fp32 across the ranks and rounded
+    once, so every rank gets the same, once-rounded sum."""
+    path = str(tmp_path / "r")
+    mp.spawn(_worker_bf16_sum, args=(2, _free_port(), path), nprocs=2, join=True)
+    (a, out0), (b, out1) = torch.load(f"{path}.0"), torch.load(f"{path}.1")
+    want = (a.float() + b.float()).to(torch.bfloat16)
+    assert torch.equal(out0, want) and torch.equal(out1, want)
