@@ -423,3 +423,21 @@ def test_shard_merge_equals_whole_vocabulary(reduction, cap):
             dh += dhp
             np.testing.assert_allclose(dwp, dw_w[:, a:b], rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(dh, dh_w, rtol=1e-11, atol=1e-13)
+
+
+def test_extreme_logits_stay_finite():
+    """Logits of +-1000 (far past exp's range) give the limits in closed form: the softmax
+    puts all mass on the largest logit, lse equals it, the entropy is 0 and the CE of a
+    label at -1000 is 2000; the gradients stay finite."""
+    hidden = np.array([[1.0]])
+    weight = np.array([[1000.0, 0.0, -1000.0]])
+    for y, ce in ((0, 0.0), (1, 1000.0), (2, 2000.0)):
+        out = orc.forward(hidden, weight, np.array([y]), "none")
+        assert out["lse"][0] == 1000.0
+        assert out["entropy_tok"][0] == 0.0
+        assert out["ce_tok"][0] == ce
+        dh, dw = orc.backward(hidden, weight, np.array([y]), out["lse"], out["ez"], [1.0], [1.0],
+                              "none")
+        assert np.all(np.isfinite(dh)) and np.all(np.isfinite(dw))
+        onehot = np.eye(3)[y]
+        np.testing.assert_allclose(dw[0], np.eye(3)[0] - onehot, atol=1e-300)
