@@ -37,16 +37,20 @@ FALLBACK_BF16_TFLOPS = 1900.0  # profiling recipe fallback (burst), used only wi
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    # about a second of timed steps on the Llama-3 head: long enough for the clock samples
+    # (every 100 ms) to describe the window
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_head")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused-memory", action="store_true",
-                    help="skip measuring the unfused PyTorch baseline's peak memory")
+                    help="skip the unfused PyTorch baseline (its peak memory and its time)")
     ap.add_argument("--no-grad-in-forward", action="store_true",
                     help="skip timing the one-call forward+backward (gradient in forward)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end run from host buffers (launch-list captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -162,7 +166,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(gpu_id)],
+                 "-lms", "100", "-i", str(gpu_id)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -183,9 +187,9 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        rows = [s for (t, s) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
-        if not rows:
-            rows = [s for (_, s) in self.samples[-3:]]
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        if not rows:  # a window shorter than the sampling interval: the nearest samples
+            rows = [s for (_, s) in sorted(self.samples, key=lambda ts: abs(ts[0] - t1))[:2]]
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -219,27 +223,66 @@ def nvsmi_id(torch, dev_index):
         return str(dev_index)
 
 
-def load_peaks(root=None):
-    """The bf16 dense peak (TFLOP/s) to report against: the measured sustained figure
-    (the kernels are timed inside long back-to-back steps), else the measured burst
-    figure, else the recipe's fallback."""
+def load_peak_table(root=None):
+    """Measured bf16 dense peaks from MEASURED_PEAKS.json: the burst and sustained
+    matmul figures (TFLOP/s) and the median SM clock seen under the sustained loop;
+    {} when the file is absent or unreadable."""
     path = os.path.join(root or ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        try:
-            d = json.load(open(path))
-            for key in ("bf16_tflops_sustained", "bf16_tflops"):
-                v = d.get(key)
-                if isinstance(v, dict):  # {"value": ..., ...}
-                    v = v.get("value", v.get("tflops"))
-                if isinstance(v, (int, float)) and v > 0:
-                    return float(v), f"of measured ({key})"
-        except (OSError, ValueError, AttributeError):
-            pass
+    if not os.path.exists(path):
+        return {}
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return {}
+    if not isinstance(d, dict):
+        return {}
+    out = {}
+    for key in ("bf16_tflops", "bf16_tflops_sustained"):
+        v = d.get(key)
+        if isinstance(v, dict):  # {"value": ..., ...}
+            v = v.get("value", v.get("tflops"))
+        if isinstance(v, (int, float)) and v > 0:
+            out[key] = float(v)
+    clk = d.get("clocks_under_load")
+    if isinstance(clk, dict) and isinstance(clk.get("sm_mhz_median"), (int, float)):
+        out["sustained_sm_mhz"] = float(clk["sm_mhz_median"])
+    return out
+
+
+def load_peaks(root=None):
+    """The bf16 dense peak (TFLOP/s) to report against: the measured burst figure (the
+    largest measured rate, so a fraction of it stays below 1), else the measured
+    sustained figure, else the recipe's fallback."""
+    t = load_peak_table(root)
+    for key in ("bf16_tflops", "bf16_tflops_sustained"):
+        if key in t:
+            return t[key], f"of measured ({key})"
     return FALLBACK_BF16_TFLOPS, "of fallback (1.9 PFLOP/s bf16 burst)"
 
 
+def roofline_fractions(achieved, sm_mhz, root=None):
+    """The achieved rate as a fraction of each measured peak, and per clock: achieved /
+    sampled SM MHz against the sustained peak / the SM MHz it was measured at (the
+    sustained loop runs power-capped at a lower clock than a short burst)."""
+    t = load_peak_table(root)
+    out = {}
+    if "bf16_tflops" in t:
+        out["frac_burst"] = achieved / t["bf16_tflops"]
+    if "bf16_tflops_sustained" in t:
+        out["frac_sustained"] = achieved / t["bf16_tflops_sustained"]
+        if sm_mhz and t.get("sustained_sm_mhz"):
+            per = achieved / sm_mhz
+            peak_per = t["bf16_tflops_sustained"] / t["sustained_sm_mhz"]
+            out["clock_normalised"] = {
+                "achieved_tflops_per_mhz": per, "peak_tflops_per_mhz": peak_per,
+                "frac": per / peak_per, "sm_mhz": sm_mhz,
+                "peak_sm_mhz": t["sustained_sm_mhz"]}
+    return out
+
+
 def load_traffic(workload):
-    """Per-launch DRAM bytes of the forward GEMM from the committed ncu summary."""
+    """Per-launch DRAM bytes of the forward GEMM from the committed ncu summary (None
+    when it has not been measured since the kernel last changed)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))
@@ -248,15 +291,13 @@ def load_traffic(workload):
         return None
 
 
-def unfused_memory(torch, w, hd, Wd, yd, gld, ged, dev):
-    """Peak bytes the unfused computation allocates above its inputs (gradients, the
-    outputs both paths produce, excluded): logits in fp32 from fp32 copies of hidden
-    and weight, log-softmax, entropy and cross-entropy as written out on the pages,
-    z-loss and soft-cap when the workload has them, and autograd's backward."""
+def unfused_step(torch, w, hd, Wd, yd, gld, ged):
+    """One forward + backward of the unfused computation: logits in fp32 from fp32
+    copies of hidden and weight, log-softmax, entropy and cross-entropy as written out
+    on the pages (verl PR #462, "Equivalent compute logic"), masking of ignored rows,
+    z-loss and soft-cap when the workload has them, and autograd's backward.  Returns
+    the two leaf tensors (their .grad hold the gradients)."""
     import torch.nn.functional as F
-    torch.cuda.synchronize()
-    base = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
     h = hd.detach().requires_grad_(True)
     W = Wd.detach().requires_grad_(True)
     logits = torch.matmul(h.float(), W.float())
@@ -275,12 +316,38 @@ def unfused_memory(torch, w, hd, Wd, yd, gld, ged, dev):
         den = valid.sum() if w.reduction == "mean" else 1.0
         obj = (loss_t.sum() * gld[0] + ent_t.sum() * ged[0]) / den
     obj.backward()
+    return h, W
+
+
+def unfused_baseline(torch, w, hd, Wd, yd, gld, ged, dev, warmup=2, steps=3):
+    """The unfused computation as a stated baseline (not the target): peak bytes it
+    allocates above its inputs (the gradients, outputs both paths produce, excluded),
+    and its time per fwd+bwd step (CUDA events, after `warmup` steps)."""
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    h, W = unfused_step(torch, w, hd, Wd, yd, gld, ged)
     torch.cuda.synchronize()
     grads = h.grad.numel() * h.grad.element_size() + W.grad.numel() * W.grad.element_size()
     peak = torch.cuda.max_memory_allocated(dev) - base - grads
-    del h, W, logits, lse, p, ent, ce, valid, loss_t, ent_t, obj
+    del h, W
+    for _ in range(warmup):
+        unfused_step(torch, w, hd, Wd, yd, gld, ged)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        unfused_step(torch, w, hd, Wd, yd, gld, ged)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
     torch.cuda.empty_cache()
-    return int(peak)
+    return {"peak_extra_bytes": int(peak), "ms_per_step": ms, "tokens_per_s": w.N / (ms / 1e3),
+            "steps": steps, "warmup": warmup,
+            "what": "verl PR #462 equivalent compute logic in PyTorch (fp32 logits, softmax, "
+                    "entropy, cross-entropy, autograd backward), masked like the fused path"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -469,19 +536,22 @@ def run_ours(args):
         del pipe
         return res
 
-    e2e_ms, e2e_med, h2d, d2h = e2e(False)
-    if gif is not None:
-        gms, gmed, _, _ = e2e(True)
-        gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
-                      "median_step_ms": gmed}
+    e2e_res = None
+    if not args.no_e2e:
+        e2e_res = e2e(False)
+        if gif is not None:
+            gms, gmed, _, _ = e2e(True)
+            gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
+                          "median_step_ms": gmed}
 
-    # the unfused baseline's memory: the pages' equivalent compute logic in plain PyTorch
-    # (fp32 logits, softmax, entropy, cross-entropy, autograd backward), run once outside
-    # every timed region; bytes above the inputs, the gradients excluded as outputs
-    unfused_peak = None
+    # the unfused baseline: the pages' equivalent compute logic in plain PyTorch (fp32
+    # logits, softmax, entropy, cross-entropy, autograd backward), run outside every
+    # timed region of the fused path; its peak memory above the inputs (the gradients
+    # excluded as outputs) and its time per step
+    unfused = None
     if not args.no_unfused_memory:
         del ws_f, ws_b
-        unfused_peak = unfused_memory(torch, w, hd, Wd, yd, gld, ged, dev)
+        unfused = unfused_baseline(torch, w, hd, Wd, yd, gld, ged, dev)
 
     ms_step = total_ms / K
     tokens = N * world
@@ -489,6 +559,8 @@ def run_ours(args):
     flops_step = 8.0 * N * H * V
     tflops = flops_step / (ms_step / 1e3) / 1e12
     peak, peak_src = load_peaks()
+    fracs = roofline_fractions(2.0 * N * H * V / (statistics.mean(fwd_ms) / 1e3) / 1e12,
+                               clocks.get("sm_mhz"))
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     fwd_tflops = 2.0 * N * H * V / (fwd_avg / 1e3) / 1e12
@@ -507,21 +579,28 @@ def run_ours(args):
                      "kernel": "flce_gemm_pair_kernel<EPI_FWD_STATS> (timed as the flce_forward call)",
                      "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": fwd_tflops / peak, "peak_note": peak_src,
+                     **fracs,
                      "algorithmic": "2*N*H*V flops per launch",
                      "traffic": load_traffic(w.name)},
         "roofline_step": {"bound": "tensor", "achieved": tflops, "peak": peak,
                           "unit": "TFLOP/s", "frac": tflops / peak,
                           "algorithmic": "8*N*H*V flops per step (fwd 2, bwd 6 incl. recompute)"},
         "memory": {"peak_extra_bytes": int(peak_extra),
-                   "unfused_peak_extra_bytes": unfused_peak,
+                   "unfused_peak_extra_bytes": unfused and unfused["peak_extra_bytes"],
                    "workspace_fwd_bytes": int(workspace_size(p, 0)),
                    "workspace_bwd_bytes": int(workspace_size(p, 1)),
                    "unfused_fp32_logits_bytes": int(N * V * 4)},
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "median_step_ms": e2e_med},
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if e2e_res is not None:
+        e2e_ms, e2e_med, h2d, d2h = e2e_res
+        out["e2e"] = {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                      "median_step_ms": e2e_med}
+    if unfused is not None:
+        unfused["speedup_of_fused"] = unfused["ms_per_step"] / ms_step
+        out["unfused_baseline"] = unfused
     if gif is not None:
         gif["speedup_vs_two_call"] = ms_step / gif["ms_per_step"]
         out["grad_in_forward"] = gif

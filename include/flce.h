@@ -211,38 +211,39 @@ int flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_
 /* Diagnostic (no counterpart on the pages): the schedule the library plans for one of
  * its GEMMs, from the GEMM's shape in tiles and the GPU's capacity; host arithmetic
  * only, usable without a GPU.
- *   m_tiles, n_tiles: output tiles (256 rows x tn columns); raster: 0 = the M tiles
+ *   m_tiles, n_tiles: output tiles (256 rows x 256 columns); raster: 0 = the M tiles
  *   vary fastest in the persistent schedule, 1 = the N tiles; panel_bytes: bytes of the
  *   operand every tile of a raster group revisits, per tile of the fast dimension;
  *   a_hint, b_hint: the L2 policy wanted for the A / B loads (0 normal, 1 evict-first,
- *   2 evict-last); clusters4, clusters2: clusters of four CTAs and CTA pairs the GPU
- *   holds at once (36 and 76 on a 152-SM GB300).
- *   out[4] receives: operand sharing (0 none, 1 two pairs along M share B, 2 two pairs
- *   along N share A), tiles of the fast dimension per raster group (in cluster tiles),
- *   and the L2 policies of the A and B loads.
+ *   2 evict-last); pairs: CTA pairs the GPU holds at once (76 on a 152-SM GB300).
+ *   out[3] receives: tiles of the fast dimension per raster group, and the L2
+ *   policies of the A and B loads.
  * Returns FLCE_OK, or FLCE_ERR_BAD_ARG for a NULL out or an out-of-range argument. */
 int flce_plan_tiles(int32_t m_tiles, int32_t n_tiles, int32_t raster, int64_t panel_bytes,
-                    int32_t tn, int32_t a_hint, int32_t b_hint, int32_t clusters4,
-                    int32_t clusters2, int32_t* out);
+                    int32_t a_hint, int32_t b_hint, int32_t pairs, int32_t* out);
 
 /* Static, NUL-terminated description of a status code. */
 const char* flce_strerror(int code);
 
 /* Forward pass for callers that cannot allocate device memory.  (The pages have
- * no counterpart: this entry point serves callers that can't call cudaMalloc,
- * e.g. code running during CUDA graph capture or under an allocator they do not
- * control, which therefore cannot provide the workspace flce_forward needs.)
- *   Same arguments and results as flce_forward, minus the workspace.  The scratch
- *   it uses is a static device array of FLCE_NOALLOC_SCRATCH_BYTES (64 MiB) held
- *   by every GPU that loads the library until the process exits; problems whose
- *   flce_workspace_size(params, 0) exceeds it return FLCE_ERR_SCRATCH_LIMIT
+ * no counterpart: this entry point serves callers that can't call cudaMalloc, e.g.
+ * code whose device memory a framework or serving runtime hands out up front and
+ * keeps, or code under an allocator it does not own, which therefore cannot
+ * provide the workspace flce_forward needs.)
+ *   Same arguments and results as flce_forward, minus the workspace, and the same
+ *   kernels in the same order, so the results are bitwise flce_forward's.  The
+ *   scratch it uses is a static device array of FLCE_NOALLOC_SCRATCH_BYTES (64 MiB)
+ *   held by every GPU that loads the library until the process exits; problems
+ *   whose flce_workspace_size(params, 0) exceeds it return FLCE_ERR_SCRATCH_LIMIT
  *   without enqueueing anything.  Nothing is allocated (no cudaMalloc/cudaFree).
  *   The first call on a device looks up the array's device address with that
  *   device current; make that first call before any stream capture.  All calls
  *   share the array (its header is cleared on every call; the rest is fully
  *   rewritten), so calls that may overlap on the GPU -- other streams, other
  *   threads -- race and must be serialised by the caller.  flce_status() is not
- *   available for it; set params->validate to get device-side errors returned. */
+ *   available for it; set params->validate to get device-side errors returned
+ *   (the call then waits for `stream` and copies the error word to the host
+ *   before it returns). */
 #define FLCE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int flce_forward_noalloc(const flce_params* params, const void* hidden, const void* weight,
                          const int64_t* labels, float* loss, float* entropy, float* lse,

@@ -98,7 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint64, vp]
         lib.flce_selftest_wait_timeout.restype = ctypes.c_int
         i32 = ctypes.c_int32
-        lib.flce_plan_tiles.argtypes = [i32, i32, i32, ctypes.c_int64, i32, i32, i32, i32, i32,
+        lib.flce_plan_tiles.argtypes = [i32, i32, i32, ctypes.c_int64, i32, i32, i32,
                                         ctypes.POINTER(i32)]
         lib.flce_plan_tiles.restype = ctypes.c_int
         lib.flce_version.argtypes = []
@@ -141,13 +141,12 @@ def workspace_size(params: FlceParams, phase: int) -> int:
     return int(n)
 
 
-def plan_tiles(m_tiles, n_tiles, raster, panel_bytes, tn=256, a_hint=0, b_hint=0,
-               clusters4=36, clusters2=76):
+def plan_tiles(m_tiles, n_tiles, raster, panel_bytes, a_hint=0, b_hint=0, pairs=76):
     """The GEMM schedule the library plans (host arithmetic, no GPU needed):
-    (share, group, a_hint, b_hint); see flce_plan_tiles in flce.h."""
-    out = (ctypes.c_int32 * 4)()
-    _check(load_library().flce_plan_tiles(m_tiles, n_tiles, raster, panel_bytes, tn, a_hint,
-                                          b_hint, clusters4, clusters2, out))
+    (group, a_hint, b_hint); see flce_plan_tiles in flce.h."""
+    out = (ctypes.c_int32 * 3)()
+    _check(load_library().flce_plan_tiles(m_tiles, n_tiles, raster, panel_bytes, a_hint,
+                                          b_hint, pairs, out))
     return tuple(out)
 
 

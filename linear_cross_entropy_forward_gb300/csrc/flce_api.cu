@@ -275,51 +275,19 @@ int raster_group(int64_t panel_bytes, int fast_tiles) {
   return g < fast_tiles ? static_cast<int>(g) : fast_tiles;
 }
 
-// Two CTA pairs per cluster share one operand (halving its L2 requests): along a
-// dimension with an even tile count (no spare tile), else along the longer one; a
-// single tile keeps one pair per cluster.  Clusters of four fit fewer pairs at once
-// (144 of 152 SMs on GB300), so with FLCE_CLUSTER_SHARE 2 (the default) they are
-// used only when the persistent schedule needs at most 6 % more rounds of tiles than
-// with one pair per cluster: the halved L2 requests lower the power draw, which
-// under the power cap buys back about that much clock; 1 always shares, 0 never.  `panel_bytes` is the revisited
-// operand's size per tile of the fast raster dimension; the group is counted in
-// cluster tiles.
-#ifndef FLCE_CLUSTER_SHARE
-#define FLCE_CLUSTER_SHARE 2
-#endif
-// The plan from the tile counts and the numbers of clusters of four (c4) and of CTA
-// pairs (c2) the GPU holds at once: host arithmetic only.
-void plan_tiles_for(GemmShape* sh, int64_t panel_bytes, int tn, int64_t c4, int64_t c2) {
-  int share = 0;
-  if (FLCE_CLUSTER_SHARE && tn == 256) {
-    if (sh->m_tiles % 2 == 0)
-      share = 1;
-    else if (sh->n_tiles % 2 == 0)
-      share = 2;
-    else if (int64_t(sh->m_tiles) * sh->n_tiles > 1)
-      share = sh->m_tiles >= sh->n_tiles ? 1 : 2;
-  }
-  if (share && FLCE_CLUSTER_SHARE == 2) {
-    const int64_t pair_tiles = int64_t(sh->m_tiles) * sh->n_tiles;
-    const int64_t quad_tiles = (share == 1 ? cdiv(sh->m_tiles, 2) * sh->n_tiles
-                                           : sh->m_tiles * cdiv(sh->n_tiles, 2));
-    if (c4 <= 0 || c2 <= 0 || cdiv(quad_tiles, c4) * 100 > cdiv(pair_tiles, c2) * 106)
-      share = 0;
-  }
-  sh->share = share;
+// The raster group and L2 policies of one GEMM, from its tile counts and the
+// number of CTA pairs (c2) the GPU holds at once: host arithmetic only.
+// `panel_bytes` is the revisited operand's size per tile of the fast raster
+// dimension.
+void plan_tiles_for(GemmShape* sh, int64_t panel_bytes, int64_t c2) {
   const bool m_fast = sh->raster == 0;
-  const int cm = share == 1 ? (sh->m_tiles + 1) / 2 : sh->m_tiles;
-  const int cn = share == 2 ? (sh->n_tiles + 1) / 2 : sh->n_tiles;
-  const bool fast_shared = m_fast ? share == 1 : share == 2;
-  const int64_t panel = panel_bytes * (fast_shared ? 2 : 1);
-  const int fast = m_fast ? cm : cn;
+  const int fast = m_fast ? sh->m_tiles : sh->n_tiles;
   // When few panels fit the L2 budget, a square-ish set of resident tiles reads
   // fewer distinct rows and columns: the k-steps of all resident tiles advance
   // together (persistent schedule), so only the k-slices in flight need to be in L2.
-  const int64_t cap = share ? c4 : c2;
   int g = 1;
-  while (int64_t(g + 1) * (g + 1) <= cap) ++g;
-  const int budget_group = raster_group(panel, fast);
+  while (int64_t(g + 1) * (g + 1) <= c2) ++g;
+  const int budget_group = raster_group(panel_bytes, fast);
   if (budget_group < g && budget_group < fast) {
     sh->group = g < fast ? g : fast;
     // No panel stays in L2 for long here: an evict_last policy would only pin
@@ -331,8 +299,8 @@ void plan_tiles_for(GemmShape* sh, int64_t panel_bytes, int tn, int64_t c4, int6
   }
 }
 
-void plan_tiles(GemmShape* sh, int64_t panel_bytes, int tn) {
-  plan_tiles_for(sh, panel_bytes, tn, cluster_capacity(4), cluster_capacity(2));
+void plan_tiles(GemmShape* sh, int64_t panel_bytes) {
+  plan_tiles_for(sh, panel_bytes, pair_capacity());
 }
 
 GemmShape base_shape(int a_hint, int b_hint) {
@@ -406,21 +374,18 @@ int flce_status(const void* workspace, void* stream) {
 }
 
 int flce_plan_tiles(int32_t m_tiles, int32_t n_tiles, int32_t raster, int64_t panel_bytes,
-                    int32_t tn, int32_t a_hint, int32_t b_hint, int32_t clusters4,
-                    int32_t clusters2, int32_t* out) {
+                    int32_t a_hint, int32_t b_hint, int32_t pairs, int32_t* out) {
   if (!out || m_tiles < 1 || n_tiles < 1 || (raster != 0 && raster != 1) || panel_bytes < 0 ||
-      tn < 1 || a_hint < 0 || a_hint > 2 || b_hint < 0 || b_hint > 2 || clusters4 < 0 ||
-      clusters2 < 1)
+      a_hint < 0 || a_hint > 2 || b_hint < 0 || b_hint > 2 || pairs < 1)
     return FLCE_ERR_BAD_ARG;
   GemmShape sh = base_shape(a_hint, b_hint);
   sh.m_tiles = m_tiles;
   sh.n_tiles = n_tiles;
   sh.raster = raster;
-  plan_tiles_for(&sh, panel_bytes, tn, clusters4, clusters2);
-  out[0] = sh.share;
-  out[1] = sh.group;
-  out[2] = sh.a_hint;
-  out[3] = sh.b_hint;
+  plan_tiles_for(&sh, panel_bytes, pairs);
+  out[0] = sh.group;
+  out[1] = sh.a_hint;
+  out[2] = sh.b_hint;
   return FLCE_OK;
 }
 
@@ -457,7 +422,7 @@ int launch_stats(const flce_params* p, const void* hidden, const void* weight,
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
   sh.a_mn_off = static_cast<int>(n0);
   sh.raster = 0;
-  plan_tiles(&sh, int64_t(PAIR_BM) * H * 2, TN_FWD);
+  plan_tiles(&sh, int64_t(PAIR_BM) * H * 2);
   EpiArgs ea{};
   ea.rows = static_cast<int>(rows);
   ea.cols = static_cast<int>(V);
@@ -701,7 +666,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s3.n_tiles = static_cast<int>(cdiv(w, TN_DLOGITS));
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
     s3.raster = 0;
-    plan_tiles(&s3, int64_t(PAIR_BM) * H * 2, TN_DLOGITS);
+    plan_tiles(&s3, int64_t(PAIR_BM) * H * 2);
     s3.b_mn_off = static_cast<int>(v0);
     EpiArgs e3{};
     e3.rows = static_cast<int>(N);
@@ -736,7 +701,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       s4.m_tiles = static_cast<int>(cdiv(w, PAIR_BM));
       s4.n_tiles = static_cast<int>(cdiv(H, TN_DWEIGHT));
       s4.raster = 1;
-      plan_tiles(&s4, int64_t(TN_DWEIGHT) * N * 2, TN_DWEIGHT);
+      plan_tiles(&s4, int64_t(TN_DWEIGHT) * N * 2);
       e4.rows = static_cast<int>(w);
       e4.cols = static_cast<int>(H);
       e4.out = static_cast<__nv_bfloat16*>(dweight) + v0 * H;
@@ -745,7 +710,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       s4.m_tiles = static_cast<int>(cdiv(H, PAIR_BM));
       s4.n_tiles = static_cast<int>(cdiv(w, TN_DWEIGHT));
       s4.raster = 0;
-      plan_tiles(&s4, int64_t(PAIR_BM) * N * 2, TN_DWEIGHT);
+      plan_tiles(&s4, int64_t(PAIR_BM) * N * 2);
       e4.rows = static_cast<int>(H);
       e4.cols = static_cast<int>(w);
       e4.col_base = static_cast<int>(v0);
@@ -763,7 +728,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));
     s5.raster = 1;
-    plan_tiles(&s5, int64_t(TN_DHIDDEN) * w * 2, TN_DHIDDEN);
+    plan_tiles(&s5, int64_t(TN_DHIDDEN) * w * 2);
     s5.b_k_off = static_cast<int>(v0);
     EpiArgs e5{};
     e5.rows = static_cast<int>(N);
@@ -888,7 +853,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(V, BK));
     s5.raster = 0;
-    plan_tiles(&s5, int64_t(PAIR_BM) * V * 2, TN_DHIDDEN);
+    plan_tiles(&s5, int64_t(PAIR_BM) * V * 2);
     EpiArgs e5{};
     e5.rows = static_cast<int>(rows);
     e5.cols = static_cast<int>(H);
@@ -913,7 +878,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
       s4.n_tiles = static_cast<int>(cdiv(H, TN_DWEIGHT));
       s4.b_k_off = static_cast<int>(n0);
       s4.raster = 1;
-      plan_tiles(&s4, int64_t(TN_DWEIGHT) * rows * 2, TN_DWEIGHT);
+      plan_tiles(&s4, int64_t(TN_DWEIGHT) * rows * 2);
       e4.rows = static_cast<int>(V);
       e4.cols = static_cast<int>(H);
     } else {
@@ -921,7 +886,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
       s4.n_tiles = static_cast<int>(cdiv(V, TN_DWEIGHT));
       s4.a_k_off = static_cast<int>(n0);
       s4.raster = 0;
-      plan_tiles(&s4, int64_t(PAIR_BM) * rows * 2, TN_DWEIGHT);
+      plan_tiles(&s4, int64_t(PAIR_BM) * rows * 2);
       e4.rows = static_cast<int>(H);
       e4.cols = static_cast<int>(V);
     }

@@ -156,27 +156,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorM
       : "memory");
 }
 
-// The same load delivered to every CTA of `cta_mask` (same shared-memory offset in
-// each).  The completion of the bytes that land in a CTA is signalled on the
-// barrier at `mbar_cluster_addr`'s offset in that CTA's pair leader when the
-// address names this CTA's leader, as it does here.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
-                                                    uint32_t mbar_cluster_addr, int32_t x,
-                                                    int32_t y, uint16_t cta_mask,
-                                                    uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(x), "r"(y),
-      "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
 // L2 policies: lines loaded with evict_last outlive evict_normal / evict_first lines.
 enum L2Hint : int { L2_NORMAL = 0, L2_EVICT_FIRST = 1, L2_EVICT_LAST = 2 };
 

@@ -2,13 +2,13 @@
 // linear cross-entropy + entropy path (verl PR #462, "Equivalent compute logic":
 // logits = hidden @ weight are never stored; every use of them is fused here).
 //
-// A CTA pair (cluster ranks 2p, 2p+1) owns 256 x TN output tiles:
+// A CTA pair (a cluster of two CTAs, ranks 0 and 1) owns 256 x TN output tiles:
 //   warp 0      TMA producer (both CTAs): this CTA's 128 rows of A and TN/2
 //               columns of B into a ring of 128B-swizzled shared-memory stages;
-//               completion is counted on the pair leader's (even rank) full barrier.
+//               completion is counted on the pair leader's (rank 0) full barrier.
 //   warp 1      UMMA issuer (leader only): 256 x TN x 16 tcgen05.mma.cta_group::2
-//               into one of 512/TN fp32 TMEM accumulators, commits multicast to
-//               the barriers of the cluster's CTAs.
+//               into one of 512/TN fp32 TMEM accumulators; each commit arrives on
+//               the same barrier of both CTAs of the pair.
 //   warps 2..   epilogue (both CTAs, 4 or 8 warps, see epi_warps): tcgen05.ld one
 //               row per thread (warp w reads TMEM lanes 32*(w%4)..+31 and, with 8
 //               warps, column half (w-2)/4 of the tile), then one of:
@@ -27,11 +27,8 @@
 //   aligned, pitches multiples of 32 bytes) are accessed 256 bits per thread; the
 //   caller's dweight / dhidden (16-byte alignment promised) 128 bits.
 //
-// A cluster holds one pair, or two pairs whose tiles lie side by side along M
-// (then they read the same B columns) or along N (the same A rows).  The shared
-// operand is fetched once per cluster: each CTA loads half of its 128-row share
-// and multicasts it to its counterpart in the other pair, which halves that
-// operand's L2 requests; a stage is released only when both pairs' UMMAs are done.
+// A cluster is exactly one pair, and every TMA load lands in the shared memory of
+// the CTA that issues it: no tile is delivered to more than one CTA.
 //
 // Operands arrive as 64-row pieces of 8 KB ({64 K, 64 rows} boxes for K-major,
 // {64 MN, 64 K} boxes of the transposed view for MN-major); operand majorness is a
@@ -123,8 +120,6 @@ struct GemmShape {
   int b_mn_off, b_k_off;      // added to B's (mn, k) tile coordinates
   uint32_t mn_lbo, mn_sbo;    // descriptor strides of MN-major operands (bytes)
   int a_hint, b_hint;         // L2 eviction priority of A / B tile loads (L2Hint)
-  int share;                  // 0: one pair per cluster; 1: two pairs along M share B;
-                              // 2: two pairs along N share A (clusters of 4 CTAs)
 };
 
 struct EpiArgs {
@@ -165,25 +160,15 @@ struct EpiArgs {
   uint32_t* err;
 };
 
-// Cluster tiles: with two pairs per cluster, a cluster tile is two pair tiles
-// along the shared dimension.
-__host__ __device__ __forceinline__ int cluster_m_tiles(const GemmShape& sh) {
-  return sh.share == 1 ? (sh.m_tiles + 1) >> 1 : sh.m_tiles;
-}
-__host__ __device__ __forceinline__ int cluster_n_tiles(const GemmShape& sh) {
-  return sh.share == 2 ? (sh.n_tiles + 1) >> 1 : sh.n_tiles;
-}
-
-// Cluster tile order.  raster 0: groups of `group` consecutive m-tiles, m fastest
-// within a group, every n-tile of the group before the next group (group >= the
-// m-tile count: plain m-fastest order).  raster 1: the same with the roles of m and
-// n swapped.  Grouping bounds how much of the operand revisited by every tile must
-// stay in L2.  The pair's own tile is then picked inside the cluster tile; it can
-// lie past the last tile when the shared dimension has an odd tile count.  (Host
-// callable too, so the order can be checked without a GPU.)
-__host__ __device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int pair,
-                                                     int& mt, int& nt) {
-  const int cm = cluster_m_tiles(sh), cn = cluster_n_tiles(sh);
+// Tile order of the persistent schedule.  raster 0: groups of `group` consecutive
+// m-tiles, m fastest within a group, every n-tile of the group before the next
+// group (group >= the m-tile count: plain m-fastest order).  raster 1: the same
+// with the roles of m and n swapped.  Grouping bounds how much of the operand
+// revisited by every tile must stay in L2.  (Host callable too, so the order can
+// be checked without a GPU.)
+__host__ __device__ __forceinline__ void tile_coords(int t, const GemmShape& sh, int& mt,
+                                                     int& nt) {
+  const int cm = sh.m_tiles, cn = sh.n_tiles;
   const bool m_major = sh.raster == 0;
   const int fast_tiles = m_major ? cm : cn;
   const int slow_tiles = m_major ? cn : cm;
@@ -197,35 +182,23 @@ __host__ __device__ __forceinline__ void tile_coords(int t, const GemmShape& sh,
   const int sl = r / gsize;
   mt = m_major ? f : sl;
   nt = m_major ? sl : f;
-  if (sh.share == 1) mt = 2 * mt + pair;
-  if (sh.share == 2) nt = 2 * nt + pair;
 }
 
 constexpr uint32_t PIECE_BYTES = 64 * BK * 2;  // 64 rows (MN) x 64 (K), either majorness
 
 // One stage of an operand: ROWS (MN) x 64 (K) as ROWS/64 pieces of 64 rows, 8 KB
-// apart (K-major: {64, 64} boxes; MN-major: {64, 64} boxes of the transposed view).
-// Shared by the cluster's two pairs (ROWS = 128), this CTA fetches only piece
-// `pair` and multicasts it to `mask` (itself and its counterpart in the other pair).
+// apart (K-major: {64, 64} boxes; MN-major: {64, 64} boxes of the transposed view),
+// all loaded into this CTA's own shared memory.
 template <bool MN, int ROWS>
 __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint32_t fb,
-                                             int mn0, int k0, bool shared, int pair,
-                                             uint16_t mask, uint64_t pol) {
+                                             int mn0, int k0, uint64_t pol) {
   static_assert(ROWS % 64 == 0, "operand rows");
-  if (ROWS == 128 && shared) {
-    uint8_t* d = dst + pair * PIECE_BYTES;
-    if constexpr (MN)
-      tma_load_2d_pair_mc(d, map, fb, mn0 + 64 * pair, k0, mask, pol);
-    else
-      tma_load_2d_pair_mc(d, map, fb, k0, mn0 + 64 * pair, mask, pol);
-  } else {
 #pragma unroll
-    for (int j = 0; j < ROWS / 64; ++j) {
-      if constexpr (MN)
-        tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, mn0 + 64 * j, k0, pol);
-      else
-        tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, k0, mn0 + 64 * j, pol);
-    }
+  for (int j = 0; j < ROWS / 64; ++j) {
+    if constexpr (MN)
+      tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, mn0 + 64 * j, k0, pol);
+    else
+      tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, k0, mn0 + 64 * j, pol);
   }
 }
 
@@ -550,13 +523,11 @@ struct Epilogue<EPI_ACCUM> {
 };
 
 // ------------------------------------------------------------------ pair kernel
-// Both producers of a pair load their halves (or, with two pairs per cluster, half of
-// the shared operand's share each, multicast to the other pair); completion is
-// counted on the pair leader's full barrier, which expects the bytes landing in both
-// of its CTAs.  Each leader's UMMA warp commits to the empty barriers of every CTA of
-// the cluster (a stage is free once every pair is done with it) and to the
-// tmem-full barriers of its own pair.  Each CTA's epilogue reads its own 128 TMEM
-// lanes (rows) and arrives on its pair leader's tmem-empty barrier.
+// Both producers of a pair load their halves; completion is counted on the pair
+// leader's full barrier, which expects the bytes landing in both CTAs.  The leader's
+// UMMA warp commits to the empty and tmem-full barriers of both CTAs.  Each CTA's
+// epilogue reads its own 128 TMEM lanes (rows) and arrives on the leader's
+// tmem-empty barrier.
 template <int EPI, bool A_MN, bool B_MN, int TN>
 __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -578,18 +549,16 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t prank = rank & 1u;  // 0: pair leader
-  const uint32_t lead = rank & ~1u;
-  const int pair = static_cast<int>(rank >> 1);
-  const uint32_t csize = cluster_nctarank();  // 2, or 4 with two pairs sharing an operand
+  const uint32_t prank = cluster_ctarank();  // 0: pair leader, 1: its peer
+  constexpr uint32_t kLead = 0;
+  constexpr uint16_t kPairMask = 0x3;  // both CTAs of the pair
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(cluster_count_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], csize / 2);  // one commit per pair leader
+      mbar_init(&empty[s], 1);  // the leader's commit
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -607,20 +576,18 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total = cluster_m_tiles(sh) * cluster_n_tiles(sh);
+  const int total = sh.m_tiles * sh.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs)
       const uint64_t pol_a = l2_policy(sh.a_hint);
       const uint64_t pol_b = l2_policy(sh.b_hint);
-      const bool share_a = sh.share == 2, share_b = sh.share == 1;
-      const uint16_t mc_mask = static_cast<uint16_t>(0x5u << prank);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl) {
         int mt, nt;
-        tile_coords(t, sh, pair, mt, nt);
+        tile_coords(t, sh, mt, nt);
         const int am0 = mt * PAIR_BM + static_cast<int>(prank) * 128 + sh.a_mn_off;
         const int bn0 = nt * TN + static_cast<int>(prank) * C::B_ROWS + sh.b_mn_off;
         for (int kb = 0; kb < sh.k_blocks; ++kb) {
@@ -628,21 +595,21 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             ok = false;
             break;
           }
-          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), lead);
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), kLead);
           if (prank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           const int k0 = kb * BK;
           load_operand<A_MN, 128>(sA + stage * C::A_BYTES, &tmA, fb, am0, k0 + sh.a_k_off,
-                                  share_a, pair, mc_mask, pol_a);
+                                  pol_a);
           load_operand<B_MN, C::B_ROWS>(sB + stage * C::B_BYTES, &tmB, fb, bn0,
-                                        k0 + sh.b_k_off, share_b, pair, mc_mask, pol_b);
+                                        k0 + sh.b_k_off, pol_b);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // drain: every stage this CTA filled has been released by the leaders' UMMAs
-      // (their commits target this CTA's barriers, so they must land before exit)
+      // drain: every stage this CTA filled has been released by the leader's UMMAs
+      // (its commits target this CTA's barriers, so they must land before exit)
       for (int i = 0; i < C::STAGES && ok; ++i) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ea.err)) break;
         if (++stage == C::STAGES) {
@@ -656,8 +623,6 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     if (lane == 0 && prank == 0) {
       // ---------------- UMMA issuer (pair leaders only)
       constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, TN, A_MN, B_MN);
-      const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
-      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
@@ -683,13 +648,13 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             bd[kk] = operand_desc<B_MN>(b_addr, kk, sh);
           }
           umma_bf16_pair_x4(d_tmem, ad, bd, IDESC, kb != 0 ? 1u : 0u);
-          umma_commit_pair(&empty[stage], all_mask);
+          umma_commit_pair(&empty[stage], kPairMask);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit_pair(&tfull[acc], pair_mask);
+        if (ok) umma_commit_pair(&tfull[acc], kPairMask);
       }
     }
     __syncwarp();
@@ -698,21 +663,20 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
-    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), lead);
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), kLead);
     int it = 0;
     for (int t = cid; t < total; t += ncl, ++it) {
       int mt, nt;
-      tile_coords(t, sh, pair, mt, nt);
+      tile_coords(t, sh, mt, nt);
       const int acc = it % C::NACC;
       const uint32_t aph = (it / C::NACC) & 1;
       if (!mbar_wait(&tfull[acc], aph, abort_flag, ea.err)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TN +
                              half * C::EPI_COLS;
-      if (mt < sh.m_tiles && nt < sh.n_tiles)  // not the spare tile of an odd count
-        Epilogue<EPI>::template run<C::EPI_CHUNKS>(
-            ea, tbase, mt * PAIR_BM + static_cast<int>(prank) * 128 + r,
-            nt * TN + half * C::EPI_COLS);
+      Epilogue<EPI>::template run<C::EPI_CHUNKS>(
+          ea, tbase, mt * PAIR_BM + static_cast<int>(prank) * 128 + r,
+          nt * TN + half * C::EPI_COLS);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -726,9 +690,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-// Host-side launcher of the pair kernel: clusters of 2 CTAs (4 when two pairs
-// share an operand), as many as can be resident at once (persistent), never more
-// than there are cluster tiles.
+// Host-side launcher of the pair kernel: clusters of 2 CTAs, as many as can be
+// resident at once (persistent), never more than there are tiles.
 template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const GemmShape& sh, const EpiArgs& ea, int max_clusters,
@@ -739,10 +702,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (sh.m_tiles <= 0 || sh.n_tiles <= 0) return cudaSuccess;
-  if (sh.share != 0 && (TN != 256 || sh.share > 2)) return cudaErrorInvalidValue;
-  const int csize = sh.share ? 4 : 2;
-  const int total = (sh.share == 1 ? (sh.m_tiles + 1) / 2 : sh.m_tiles) *
-                    (sh.share == 2 ? (sh.n_tiles + 1) / 2 : sh.n_tiles);
+  constexpr int csize = 2;
+  const int total = sh.m_tiles * sh.n_tiles;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
@@ -759,10 +720,9 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, sh, ea);
 }
 
-// Largest number of co-resident clusters of `csize` CTAs of this kernel on the
-// current device.
+// Largest number of co-resident CTA pairs of this kernel on the current device.
 template <int EPI, bool A_MN, bool B_MN, int TN>
-cudaError_t pair_max_clusters(int csize, int* out) {
+cudaError_t pair_max_clusters(int* out) {
   using C = PairCfg<TN, epi_warps<EPI>()>;
   auto kern = flce_gemm_pair_kernel<EPI, A_MN, B_MN, TN>;
   cudaError_t e =
@@ -770,11 +730,11 @@ cudaError_t pair_max_clusters(int csize, int* out) {
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(csize, 1, 1);
+  cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(pair_threads<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.attrs = attr;
@@ -782,32 +742,29 @@ cudaError_t pair_max_clusters(int csize, int* out) {
   return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
 }
 
-// Launch with the co-resident cluster count of this instantiation and cluster
-// size, queried once per device (the query needs the kernel's attributes set, so
-// it is cached here).
+// Launch with the co-resident pair count of this instantiation, queried once per
+// device (the query needs the kernel's attributes set, so it is cached here).
 template <int EPI, bool A_MN, bool B_MN, int TN>
 cudaError_t launch_pair_cached(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                const GemmShape& sh, const EpiArgs& ea, cudaStream_t stream) {
-  static std::atomic<int> max_clusters[64][2];
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int four = sh.share != 0;
-  int mc = max_clusters[dev][four].load();
+  int mc = max_clusters[dev].load();
   if (mc <= 0) {
-    e = pair_max_clusters<EPI, A_MN, B_MN, TN>(four ? 4 : 2, &mc);
+    e = pair_max_clusters<EPI, A_MN, B_MN, TN>(&mc);
     if (e != cudaSuccess) return e;
     if (mc <= 0) return cudaErrorInvalidConfiguration;
-    max_clusters[dev][four].store(mc);
+    max_clusters[dev].store(mc);
   }
   return launch_gemm_pair<EPI, A_MN, B_MN, TN>(tmA, tmB, sh, ea, mc, stream);
 }
 
-// Clusters of `csize` (2 or 4) CTAs that fit on the current device at once; every
-// pair kernel takes a whole SM's shared memory, so one query serves them all.
-// 0 if the query fails.
-int cluster_capacity(int csize);
+// CTA pairs that fit on the current device at once; every pair kernel takes a
+// whole SM's shared memory, so one query serves them all.  0 if the query fails.
+int pair_capacity();
 
 // Launchers of the instantiations the path uses (one translation unit each).
 #define FLCE_DECLARE_LAUNCHER(name)                                                  \

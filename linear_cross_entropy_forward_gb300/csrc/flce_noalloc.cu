@@ -1,8 +1,8 @@
 // flce_forward_noalloc: the forward pass for callers that cannot allocate device
-// memory.  It has no counterpart in the pages; it exists because some callers
-// can't call cudaMalloc: code running while a CUDA graph is being captured,
-// inside a memory pool they do not own, or under an allocator that is locked
-// for a step (custom-allocator runtimes, embedded inference servers).
+// memory.  It has no counterpart in the pages; it exists because some callers can't
+// call cudaMalloc: a framework or serving runtime may hand out all device memory up
+// front and keep it, or the caller may run under an allocator it does not own, and
+// then there is no way to provide the workspace flce_forward needs.
 //
 // Instead of a caller-supplied workspace it uses the file-scope device array
 // below, FLCE_NOALLOC_SCRATCH_BYTES (64 MiB) per GPU.  Every GPU that loads this

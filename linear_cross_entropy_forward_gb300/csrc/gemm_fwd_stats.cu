@@ -4,15 +4,14 @@
 namespace flce {
 FLCE_DEFINE_LAUNCHER(launch_fwd_stats, EPI_FWD_STATS, false, true, TN_FWD)
 
-int cluster_capacity(int csize) {
-  static std::atomic<int> cap[64][2];
+int pair_capacity() {
+  static std::atomic<int> cap[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int k = csize == 4 ? 1 : 0;
-  int c = cap[dev][k].load();
+  int c = cap[dev].load();
   if (c <= 0) {
-    if (pair_max_clusters<EPI_FWD_STATS, false, true, TN_FWD>(csize, &c) != cudaSuccess) return 0;
-    cap[dev][k].store(c);
+    if (pair_max_clusters<EPI_FWD_STATS, false, true, TN_FWD>(&c) != cudaSuccess) return 0;
+    cap[dev].store(c);
   }
   return c;
 }

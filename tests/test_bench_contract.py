@@ -64,8 +64,42 @@ def test_peak_comes_from_the_measured_file_when_present(tmp_path):
     assert bench.load_peaks(str(tmp_path)) == (1900.0, "of fallback (1.9 PFLOP/s bf16 burst)")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
         {"hbm_gbs": 7100.0, "bf16_tflops": 2050.0, "bf16_tflops_sustained": 1720.0}))
+    # the burst figure is the larger measured rate: the peak a fraction is taken of
+    assert bench.load_peaks(str(tmp_path)) == (2050.0, "of measured (bf16_tflops)")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops_sustained": 1720.0}))
     assert bench.load_peaks(str(tmp_path)) == (1720.0, "of measured (bf16_tflops_sustained)")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": {"value": 2010.0}}))
     assert bench.load_peaks(str(tmp_path)) == (2010.0, "of measured (bf16_tflops)")
     (tmp_path / "MEASURED_PEAKS.json").write_text("not json")
     assert bench.load_peaks(str(tmp_path))[0] == 1900.0
+
+
+def test_roofline_fractions_against_burst_sustained_and_per_clock(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0,
+         "clocks_under_load": {"sm_mhz_median": 1600.0}}))
+    f = bench.roofline_fractions(1800.0, 2000.0, str(tmp_path))
+    assert abs(f["frac_burst"] - 0.9) < 1e-12
+    assert abs(f["frac_sustained"] - 1.125) < 1e-12
+    cn = f["clock_normalised"]
+    # 1800 TF/s at 2000 MHz is 0.9 TF/s per MHz; the sustained peak is 1.0 per MHz
+    assert abs(cn["achieved_tflops_per_mhz"] - 0.9) < 1e-12
+    assert abs(cn["peak_tflops_per_mhz"] - 1.0) < 1e-12
+    assert abs(cn["frac"] - 0.9) < 1e-12
+    # no sampled clock: no per-clock fraction; no file: nothing
+    assert "clock_normalised" not in bench.roofline_fractions(1800.0, None, str(tmp_path))
+    assert bench.roofline_fractions(1800.0, 2000.0, str(tmp_path / "absent")) == {}
+
+
+def test_reported_peak_is_the_largest_measured_rate():
+    """The roofline's `peak` is the burst figure when both are measured, so `frac`
+    (achieved / peak) can exceed 1 only if the kernel beat the burst matmul itself."""
+    sys.path.insert(0, ROOT)
+    import bench
+    t = bench.load_peak_table()
+    if "bf16_tflops" not in t:
+        return
+    peak, _ = bench.load_peaks()
+    assert peak == max(v for k, v in t.items() if k.startswith("bf16_tflops"))

@@ -1,13 +1,12 @@
 """The GEMM schedule planner (flce_plan_tiles), on the CPU.
 
 The expected plans are derived by hand from the stated policy; each case gives the
-derivation. GB300 holds 36 clusters of four CTAs or 76 CTA pairs at once, and tiles
-are 256 x 256.
-- Two pairs share an operand along an even tile dimension (else along the longer one)
-  unless that needs more than 6 % more rounds of tiles.
+derivation.  GB300 holds 76 CTA pairs at once (one pair per cluster), tiles are
+256 x 256, and the square side of a resident set of 76 tiles is 8 (8^2 <= 76 < 9^2).
 - Raster groups keep the revisited operand's panels within 40 MiB of L2.
-- When fewer panels than a square-ish resident set fit that budget, the group is that
-  square (side g with g^2 <= capacity) and both operands take the normal L2 policy.
+- When fewer panels than the square side fit that budget (and fewer than the fast
+  dimension has), the group is that square side (capped at the fast dimension) and
+  both operands take the normal L2 policy.
 """
 import pytest
 
@@ -24,54 +23,54 @@ def _lib():
 
 
 CASES = [
-    # Llama-3 head forward: 32 x 501 tiles, hidden panels 256 x 4096 x 2 B = 2 MiB.
-    # M even -> share B; 8016 cluster tiles take ceil(8016/36) = 223 rounds against
-    # ceil(16032/76) = 211 for pairs: 223 <= 1.06 * 211, so share.  A shared panel is
-    # 4 MiB: 10 fit 40 MiB, >= the square side 6 (36 clusters) -> group 10, hints kept.
-    ("llama3_forward", (32, 501, 0, 2 * MiB, 256, EVICT_LAST, NORMAL), (1, 10, EVICT_LAST, NORMAL)),
-    # Llama-3 dlogits, first 65536-column chunk: 32 x 256 tiles; 114 rounds against 108
-    # (<= 6 % more) -> share; group 10 as above.
-    ("llama3_dlogits", (32, 256, 0, 2 * MiB, 256, EVICT_LAST, NORMAL), (1, 10, EVICT_LAST, NORMAL)),
-    # Llama-3 dweight [H,V], first chunk: 16 x 256 tiles, hidden^T panels 256 x 8192 x 2 B =
-    # 4 MiB; 57 rounds against 54 -> share.  Shared panels of 8 MiB: 5 fit, fewer than
-    # the square side 6 and than the 8 fast cluster tiles -> lockstep group 6, normal hints.
-    ("llama3_dweight", (16, 256, 0, 4 * MiB, 256, EVICT_LAST, NORMAL), (1, 6, NORMAL, NORMAL)),
+    # Llama-3 head forward: 32 x 501 tiles, M fastest, hidden panels 256 x 4096 x 2 B =
+    # 2 MiB: 20 fit 40 MiB, fewer than the 32 M tiles but not fewer than the square
+    # side 8 -> group 20, hints kept.
+    ("llama3_forward", (32, 501, 0, 2 * MiB, EVICT_LAST, NORMAL), (20, EVICT_LAST, NORMAL)),
+    # Llama-3 dlogits, first 65536-column chunk: 32 x 256 tiles, same panels -> 20.
+    ("llama3_dlogits", (32, 256, 0, 2 * MiB, EVICT_LAST, NORMAL), (20, EVICT_LAST, NORMAL)),
+    # Llama-3 dweight [H,V], first chunk: 16 x 256 tiles, hidden^T panels 256 x 8192 x
+    # 2 B = 4 MiB: 10 fit, >= 8 -> group 10, hints kept.
+    ("llama3_dweight", (16, 256, 0, 4 * MiB, EVICT_LAST, NORMAL), (10, EVICT_LAST, NORMAL)),
     # Llama-3 dhidden, first chunk: 32 x 16 tiles, N fastest, weight panels 256 x 65536 x
-    # 2 B = 32 MiB.  Sharing: 8 rounds of clusters against 7 of pairs (+14 %) -> none.
-    # One panel fits; square side for 76 pairs is 8 -> lockstep group 8, normal hints.
-    ("llama3_dhidden", (32, 16, 1, 32 * MiB, 256, NORMAL, EVICT_LAST), (0, 8, NORMAL, NORMAL)),
-    # Gemma-2 dweight [H,V], first 131072-column chunk: 9 x 512 tiles.  M odd, N even ->
-    # share A along N; 64 rounds against 61 (<= 6 %).  The fast M dimension is not the
-    # shared one: panels 256 x 4096 x 2 B = 2 MiB, 20 fit, capped at the 9 M tiles.
-    ("gemma_dweight", (9, 512, 0, 2 * MiB, 256, EVICT_LAST, NORMAL), (2, 9, EVICT_LAST, NORMAL)),
-    # Both counts odd: share along the longer dimension (N); 1 round either way.
-    ("odd_counts", (3, 5, 0, 1 * MiB, 256, NORMAL, NORMAL), (2, 3, NORMAL, NORMAL)),
-    # One tile: nothing to share.
-    ("single_tile", (1, 1, 0, 1 * MiB, 256, NORMAL, NORMAL), (0, 1, NORMAL, NORMAL)),
-    # 2 x 76 tiles: 2 rounds of pairs against 3 of clusters (+50 %) -> no sharing.
-    ("quantised", (2, 76, 1, 1 * MiB, 256, NORMAL, NORMAL), (0, 40, NORMAL, NORMAL)),
-    # 128-column tiles never share (clusters of four are built for 256-column tiles).
-    ("narrow_tiles", (32, 64, 0, 1 * MiB, 128, NORMAL, NORMAL), (0, 32, NORMAL, NORMAL)),
+    # 2 B = 32 MiB: one fits, fewer than 8 and than the 16 N tiles -> lockstep group 8,
+    # normal hints.
+    ("llama3_dhidden", (32, 16, 1, 32 * MiB, NORMAL, EVICT_LAST), (8, NORMAL, NORMAL)),
+    # Gemma-2 dweight [H,V], first 131072-column chunk: 9 x 512 tiles, M fastest, panels
+    # 256 x 4096 x 2 B = 2 MiB: 20 fit, capped at the 9 M tiles.
+    ("gemma_dweight", (9, 512, 0, 2 * MiB, EVICT_LAST, NORMAL), (9, EVICT_LAST, NORMAL)),
+    # Small odd counts: 40 panels fit, capped at the 3 M tiles.
+    ("odd_counts", (3, 5, 0, 1 * MiB, NORMAL, NORMAL), (3, NORMAL, NORMAL)),
+    # One tile.
+    ("single_tile", (1, 1, 0, 1 * MiB, NORMAL, NORMAL), (1, NORMAL, NORMAL)),
+    # N fastest over 76 tiles with 1 MiB panels: 40 fit, >= 8 -> group 40.
+    ("wide_fast_dimension", (2, 76, 1, 1 * MiB, NORMAL, NORMAL), (40, NORMAL, NORMAL)),
+    # 40 MiB panels: one fits, fewer than the square side and than the 3 fast tiles ->
+    # the square side capped at the fast dimension, 3; normal hints.
+    ("few_fast_tiles", (4, 3, 1, 40 * MiB, NORMAL, EVICT_LAST), (3, NORMAL, NORMAL)),
+    # No revisited operand (panel 0): one group over the whole fast dimension.
+    ("no_panel", (32, 501, 0, 0, EVICT_LAST, NORMAL), (32, EVICT_LAST, NORMAL)),
 ]
 
 
 @pytest.mark.parametrize("name,args,want", CASES, ids=[c[0] for c in CASES])
 def test_plan_matches_the_policy(name, args, want):
-    m, n, raster, panel, tn, ah, bh = args
-    assert B.plan_tiles(m, n, raster, panel, tn, ah, bh, 36, 76) == want
+    m, n, raster, panel, ah, bh = args
+    assert B.plan_tiles(m, n, raster, panel, ah, bh, 76) == want
 
 
-def test_plan_without_clusters_of_four_never_shares():
-    # a GPU that fits no cluster of four (capacity 0) keeps one pair per cluster
-    assert B.plan_tiles(32, 501, 0, 2 * MiB, 256, EVICT_LAST, NORMAL, 0, 76)[0] == 0
+def test_plan_with_one_pair_keeps_the_budget_group():
+    # one resident pair: the square side is 1, never above the budget group, so the
+    # budget group (1 here) and the requested hints stand
+    assert B.plan_tiles(32, 16, 1, 32 * MiB, NORMAL, EVICT_LAST, 1) == (1, NORMAL, EVICT_LAST)
 
 
-@pytest.mark.parametrize("bad", [dict(m=0), dict(n=0), dict(raster=2), dict(ah=3), dict(c2=0)])
+@pytest.mark.parametrize("bad", [dict(m=0), dict(n=0), dict(raster=2), dict(ah=3), dict(pairs=0)])
 def test_plan_rejects_bad_arguments(bad):
-    a = dict(m=4, n=4, raster=0, ah=0, c2=76)
+    a = dict(m=4, n=4, raster=0, ah=0, pairs=76)
     a.update(bad)
     with pytest.raises(B.FlceError) as ei:
-        B.plan_tiles(a["m"], a["n"], a["raster"], MiB, 256, a["ah"], 0, 36, a["c2"])
+        B.plan_tiles(a["m"], a["n"], a["raster"], MiB, a["ah"], 0, a["pairs"])
     assert ei.value.code == 1
 
 
@@ -81,34 +80,21 @@ TILE_ORDER_CHECK = r"""
 #include "flce_gemm.cuh"
 using namespace flce;
 
-// Every output tile is visited exactly once over all cluster tiles and pairs; a tile
-// past the end appears only for the spare half of a cluster tile along an odd shared
-// dimension.
-static int check(int m, int n, int share, int raster, int group) {
+// Every output tile is visited exactly once over the schedule's tile indices.
+static int check(int m, int n, int raster, int group) {
   GemmShape sh{};
-  sh.m_tiles = m; sh.n_tiles = n; sh.share = share; sh.raster = raster; sh.group = group;
-  const int total = cluster_m_tiles(sh) * cluster_n_tiles(sh);
-  const int pairs = share ? 2 : 1;
+  sh.m_tiles = m; sh.n_tiles = n; sh.raster = raster; sh.group = group;
+  const int total = m * n;
   std::vector<int> hits(static_cast<size_t>(m) * n, 0);
-  int spare = 0;
-  for (int t = 0; t < total; ++t)
-    for (int p = 0; p < pairs; ++p) {
-      int mt, nt;
-      tile_coords(t, sh, p, mt, nt);
-      if (mt < 0 || nt < 0) return 1;
-      if (mt >= m || nt >= n) {
-        const bool ok = (share == 1 && (m & 1) && mt == m && nt < n) ||
-                        (share == 2 && (n & 1) && nt == n && mt < m);
-        if (!ok) return 2;
-        ++spare;
-        continue;
-      }
-      ++hits[static_cast<size_t>(mt) * n + nt];
-    }
+  for (int t = 0; t < total; ++t) {
+    int mt, nt;
+    tile_coords(t, sh, mt, nt);
+    if (mt < 0 || nt < 0 || mt >= m || nt >= n) return 1;
+    ++hits[static_cast<size_t>(mt) * n + nt];
+  }
   for (int h : hits)
-    if (h != 1) return 3;
-  const int want_spare = share == 1 ? (m & 1) * n : share == 2 ? (n & 1) * m : 0;
-  return spare == want_spare ? 0 : 4;
+    if (h != 1) return 2;
+  return 0;
 }
 
 int main() {
@@ -117,18 +103,16 @@ int main() {
   long cases = 0;
   for (int m : dims)
     for (int n : dims)
-      for (int share = 0; share < 3; ++share)
-        for (int raster = 0; raster < 2; ++raster)
-          for (int g : groups) {
-            const int rc = check(m, n, share, raster, g);
-            if (rc) {
-              std::printf("FAIL %d m=%d n=%d share=%d raster=%d group=%d\n", rc, m, n, share,
-                          raster, g);
-              return 1;
-            }
-            ++cases;
+      for (int raster = 0; raster < 2; ++raster)
+        for (int g : groups) {
+          const int rc = check(m, n, raster, g);
+          if (rc) {
+            std::printf("FAIL %d m=%d n=%d raster=%d group=%d\\n", rc, m, n, raster, g);
+            return 1;
           }
-  std::printf("OK %ld\n", cases);
+          ++cases;
+        }
+  std::printf("OK %ld\\n", cases);
   return 0;
 }
 """
@@ -136,8 +120,8 @@ int main() {
 
 def test_tile_order_covers_every_tile_once(tmp_path):
     """The persistent schedule's tile order (tile_coords, compiled for the host with
-    nvcc): every output tile exactly once for every share, raster and group choice,
-    including ragged groups and odd shared dimensions."""
+    nvcc): every output tile exactly once for every raster and group choice,
+    including ragged groups."""
     import os
     import subprocess
     from linear_cross_entropy_forward_gb300.build import CSRC, ROOT, nvcc_path
