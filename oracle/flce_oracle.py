@@ -136,8 +136,13 @@ def label_logits(hidden, weight, labels, valid, softcap=0.0):
 
 
 def forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
-            zloss_coef=0.0, softcap=0.0, v_chunk=8192, label_smoothing=0.0, class_weight=None):
+            zloss_coef=0.0, softcap=0.0, v_chunk=8192, label_smoothing=0.0, class_weight=None,
+            stats=None):
     """Loss and entropy of verl PR #462's compute logic, with the Liger options.
+
+    ``stats``: the (lse, ez, sw) that :func:`row_stats` returns for these hidden,
+    weight, softcap and class_weight, when the caller already has them (they do not
+    depend on the labels); None computes them here.
 
     Returns a dict:
       loss, entropy   -- reduced ('mean'/'sum': float; 'none': [N] arrays)
@@ -151,7 +156,11 @@ def forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_INDEX,
     N, H, V, lab, valid = _check(hidden, weight, labels, reduction, ignore_index)
     cw = _class_weights(class_weight, V)
     eps = float(label_smoothing)
-    lse, ez, sw = row_stats(hidden, weight, softcap, v_chunk, class_weight)
+    if stats is None:
+        stats = row_stats(hidden, weight, softcap, v_chunk, class_weight)
+    lse, ez, sw = (np.asarray(a, dtype=np.float64) for a in stats)
+    if lse.shape != (N,) or ez.shape != (N,) or sw.shape != (N,):
+        raise ValueError("stats must hold three [N] arrays")
     zy = label_logits(hidden, weight, lab, valid, softcap)
     wy = np.where(valid, cw[np.where(valid, lab, 0)], 0.0)
     # cross-entropy part: (1 - eps) w_y (lse - z_y) + eps/V (W lse - sum_c w_c z_c)
@@ -223,12 +232,16 @@ def dlogits_chunk(hidden, weight, labels, lse, ez, gc, gl, ge, v0, v1,
 
 def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
              ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, v_chunk=8192,
-             rows=None, label_smoothing=0.0, class_weight=None, v_offset=0, v_total=None):
+             rows=None, label_smoothing=0.0, class_weight=None, v_offset=0, v_total=None,
+             cols=None):
     """(dhidden, dweight) in fp64.
 
     ``lse``/``ez`` must come from :func:`forward` on the same inputs.  With
     ``rows`` given, only dhidden[rows] is formed (dweight is then None): each
-    dhidden row needs only its own row of the logits.  With a vocabulary shard
+    dhidden row needs only its own row of the logits.  With ``cols`` given, only
+    the columns dweight[:, cols] are formed, over every row (dhidden is then None):
+    each dweight column needs only its own column of the logits, and every row's
+    lse and E_p[z].  With a vocabulary shard
     (weight = columns [v_offset, v_offset + V) of v_total, lse / ez of the whole
     vocabulary) the result is the shard's dweight and its term of dhidden.
     """
@@ -243,6 +256,18 @@ def backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean
     gc, gl, ge = grad_scales(g_loss, g_entropy, valid, reduction, w_valid)
     opts = dict(zloss_coef=zloss_coef, softcap=softcap, label_smoothing=label_smoothing,
                 class_weight=class_weight, v_offset=v_offset)
+    if rows is not None and cols is not None:
+        raise ValueError("give rows or cols, not both")
+    if cols is not None:
+        cols = np.asarray(cols, dtype=np.int64).reshape(-1)
+        if np.any((cols < 0) | (cols >= V)):
+            raise ValueError("column out of range")
+        dw = np.zeros((H, cols.size))
+        for i, c in enumerate(cols):
+            dz = dlogits_chunk(hidden, weight, lab, lse, ez, gc, gl, ge, int(c), int(c) + 1,
+                               **opts)
+            dw[:, i] = hidden.T @ dz[:, 0]
+        return None, dw
     if rows is not None:
         rows = np.asarray(rows, dtype=np.int64)
         hs, ls, vs = hidden[rows], lab[rows], valid[rows]

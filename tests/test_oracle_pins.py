@@ -298,6 +298,65 @@ def test_rows_subset_backward_equals_full():
     np.testing.assert_allclose(dhr, dh[rows], rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("reduction", REDS)
+@pytest.mark.parametrize("opts", [dict(), dict(zloss_coef=0.01, softcap=2.0),
+                                  dict(label_smoothing=0.1, class_weight="random")],
+                         ids=["plain", "zloss_softcap", "smooth_weighted"])
+def test_column_subset_backward_equals_full(reduction, opts):
+    """dweight[:, cols] over every row (the form the full-size GPU checks use) equals the
+    columns of the complete dweight, itself pinned by finite differences above."""
+    hidden, weight, labels = _rand_case(12, 5, 30, 23, ignore=(2, 9))
+    kw = dict(opts)
+    if kw.get("class_weight") == "random":
+        kw["class_weight"] = np.random.default_rng(5).uniform(0.5, 2.0, 30)
+    gl, ge = _grads(reduction, 12, 23)
+    out = orc.forward(hidden, weight, labels, reduction, **kw)
+    _, dw = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, reduction, **kw)
+    cols = np.array([0, int(labels[0]), 29, 17, int(labels[5])])
+    none, dwc = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, reduction,
+                             cols=cols, **kw)
+    assert none is None and dwc.shape == (5, cols.size)
+    np.testing.assert_allclose(dwc, dw[:, cols], rtol=1e-12, atol=1e-14)
+    with pytest.raises(ValueError):
+        orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, reduction,
+                     cols=[30], **kw)
+
+
+def test_column_subset_matches_finite_differences():
+    """Each returned dweight column against central differences of the objective in the
+    entries of that weight column (soft-cap and z-loss on, mean reduction)."""
+    hidden, weight, labels = _rand_case(6, 4, 20, 31)
+    kw = dict(zloss_coef=0.05, softcap=1.5)
+    gl, ge = np.array([0.8]), np.array([-0.6])
+    out = orc.forward(hidden, weight, labels, "mean", **kw)
+    cols = np.array([int(labels[0]), 3, 19])
+    _, dwc = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, "mean",
+                          cols=cols, **kw)
+    eps = 1e-6
+    fd = np.zeros_like(dwc)
+    for i, c in enumerate(cols):
+        for h in range(4):
+            wp, wm = weight.copy(), weight.copy()
+            wp[h, c] += eps
+            wm[h, c] -= eps
+            fd[h, i] = (orc.objective(hidden, wp, labels, gl, ge, "mean", **kw)
+                        - orc.objective(hidden, wm, labels, gl, ge, "mean", **kw)) / (2 * eps)
+    assert np.abs(dwc - fd).max() / max(1.0, np.abs(fd).max()) < 1e-6
+
+
+def test_forward_with_given_row_stats_equals_plain_forward():
+    hidden, weight, labels = _rand_case(9, 6, 25, 41)
+    cw = np.random.default_rng(6).uniform(0.5, 2.0, 25)
+    kw = dict(zloss_coef=0.02, softcap=3.0, label_smoothing=0.05, class_weight=cw)
+    plain = orc.forward(hidden, weight, labels, "none", **kw)
+    st = orc.row_stats(hidden, weight, 3.0, class_weight=cw)
+    given = orc.forward(hidden, weight, labels, "none", stats=st, **kw)
+    for k in ("loss", "entropy", "lse", "ez"):
+        np.testing.assert_array_equal(np.asarray(given[k]), np.asarray(plain[k]))
+    with pytest.raises(ValueError):
+        orc.forward(hidden, weight, labels, "none", stats=(st[0][:3], st[1], st[2]), **kw)
+
+
 # --------------------------------------------------------------------------- brute force
 @pytest.mark.parametrize("reduction", REDS)
 @pytest.mark.parametrize("zc,cap", [(0.0, 0.0), (0.05, 0.0), (0.0, 2.0), (0.05, 2.0)])
