@@ -43,6 +43,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_head")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="reduced case: replace the workload's N (for small ncu captures)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="reduced case: replace the workload's V (for small ncu captures)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused-memory", action="store_true",
@@ -51,6 +55,8 @@ def parse_args():
                     help="skip timing the one-call forward+backward (gradient in forward)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end run from host buffers (launch-list captures)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the two-call step of the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -102,6 +108,18 @@ def workload_config(w, world):
             "zloss_coef": w.zloss_coef, "softcap": w.softcap, "ignore_frac": w.ignore_frac,
             "label_mode": w.label_mode, "grad_mode": w.grad_mode, "global_batch": w.N * world,
             "seq_len": w.N, "parallelism": "replicas" if world > 1 else "single", "l2": l2}
+
+
+def select_workload(args):
+    """The named workload, or a reduced case of it when --tokens / --vocab are given
+    (same recipe, other sizes; its name says so)."""
+    from linear_cross_entropy_forward_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.tokens or args.vocab:
+        N = args.tokens or w.N
+        V = args.vocab or w.V
+        w = w.scaled(f"{w.name}_N{N}_V{V}", N, w.H, V)
+    return w
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -350,6 +368,64 @@ def unfused_baseline(torch, w, hd, Wd, yd, gld, ged, dev, warmup=2, steps=3):
                     "entropy, cross-entropy, autograd backward), masked like the fused path"}
 
 
+def time_other_workload(torch, w, steps, warmup, dev, local):
+    """The two-call step (flce_forward + flce_backward) of another workload: the same
+    timing and clock sampling as the headline line's, nothing else."""
+    from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward, make_params,
+                                                    workspace_size)
+    from linear_cross_entropy_forward_gb300.workloads import make_inputs
+    label_dev = "cuda" if w.label_mode == "self" else "cpu"
+    hidden, weight, labels, g_loss, g_ent = make_inputs(w, label_device=label_dev)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    gld, ged = g_loss.to(dev), g_ent.to(dev)
+    del hidden, weight
+    N, H, V = w.N, w.H, w.V
+    n_out = N if w.reduction == "none" else 1
+    out_f = (torch.empty(n_out, device=dev), torch.empty(n_out, device=dev),
+             torch.empty(N, device=dev), torch.empty(N, device=dev))
+    out_b = (torch.empty(N, H, dtype=torch.bfloat16, device=dev),
+             torch.empty(H, V, dtype=torch.bfloat16, device=dev))
+    p = make_params(N, H, V, w.reduction, zloss_coef=w.zloss_coef, softcap=w.softcap)
+    ws_f = torch.empty(workspace_size(p, 0), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(workspace_size(p, 1), dtype=torch.uint8, device=dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if needs_flush(w) else None
+
+    def step():
+        flce_forward(hd, Wd, yd, w.reduction, workspace=ws_f, out=out_f, **kw)
+        flce_backward(hd, Wd, yd, out_f[2], out_f[3], gld, ged, w.reduction, workspace=ws_b,
+                      out=out_b, **kw)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(nvsmi_id(torch, local))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = time.time()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 255)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    tflops = 8.0 * N * H * V / (ms / 1e3) / 1e12
+    peak, _ = load_peaks()
+    clocks = sampler.summary(t0, t1)
+    res = {"N": N, "H": H, "V": V, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
+           "tflops": tflops, "frac_of_peak": tflops / peak, "clocks": clocks,
+           "steps": steps, "warmup": warmup,
+           "l2": "flushed between steps" if flush is not None else "inputs larger than L2"}
+    del hd, Wd, yd, out_f, out_b, ws_f, ws_b, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -373,7 +449,7 @@ def run_ours(args):
         pg.barrier()
     build()  # no-op once built; loads nothing yet
 
-    w = WORKLOADS[args.workload]
+    w = select_workload(args)
     label_dev = "cuda" if w.label_mode == "self" else "cpu"
     hidden, weight, labels, g_loss, g_ent = make_inputs(w, label_device=label_dev)
     hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
@@ -606,7 +682,15 @@ def run_ours(args):
         out["grad_in_forward"] = gif
     if gif is not None:
         out["memory"]["grad_in_forward_extra_bytes"] = gif["workspace_bytes"]
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_other_workloads and not (args.tokens or args.vocab):
+        # the other workloads' two-call step, measured the same way (no e2e, no baselines)
+        from linear_cross_entropy_forward_gb300.workloads import WORKLOADS
+        others = {}
+        for name, ow in WORKLOADS.items():
+            if name == w.name:
+                continue
+            others[name] = time_other_workload(torch, ow, args.steps, args.warmup, dev, local)
+        out["other_workloads"] = others
         out["cpu_baseline"] = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
                                            args.cpu_seconds)
     if rank == 0:
@@ -621,8 +705,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from linear_cross_entropy_forward_gb300.workloads import WORKLOADS, make_inputs
-    w = WORKLOADS[args.workload]
+    from linear_cross_entropy_forward_gb300.workloads import make_inputs
+    w = select_workload(args)
     if w.label_mode == "self":
         import torch
         label_dev = "cuda" if torch.cuda.is_available() else "cpu"

@@ -34,8 +34,9 @@
  *   - All tensor pointers are DEVICE pointers to dense row-major arrays, owned by
  *     the caller; the library allocates no device memory and keeps no state
  *     between calls apart from a per-device cache of kernel attributes.
- *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns); weight and
- *     dweight are [H,V] or [V,H] as params->weight_layout says.
+ *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns; dhidden fp32
+ *     when params->dhidden_fp32 is set); weight and dweight are [H,V] or [V,H] as
+ *     params->weight_layout says.
  *     labels: int64.  Everything else: fp32.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *     enqueued asynchronously on it; nothing synchronises unless params->validate
@@ -45,9 +46,10 @@
  *     conditions (a label outside [0,V) that is not ignore_index, a pipeline wait
  *     that timed out) are recorded in an error word inside the workspace; they
  *     are returned by flce_status(), or directly when params->validate != 0.
- *   - Requirements: N >= 0, H >= 8, V >= 1, H % 8 == 0, V % 8 == 0 (16-byte row
- *     strides for the TMA engine); every tensor pointer 16-byte aligned (g_loss,
- *     g_entropy and class_weight: 4-byte), every workspace 256-byte aligned.
+ *   - Requirements: N >= 0, H >= 8, V >= 1, H % 8 == 0, and V % 8 == 0 for a [H,V]
+ *     weight (16-byte row strides for the TMA engine; a [V,H] weight takes any V); every tensor pointer 16-byte aligned (g_loss,
+ *     g_entropy and class_weight: 4-byte; an fp32 dhidden: 32-byte), every workspace
+ *     256-byte aligned.
  */
 #ifndef FLCE_H_
 #define FLCE_H_
@@ -78,13 +80,16 @@ enum {
   FLCE_OK = 0,
   FLCE_ERR_BAD_ARG = 1,       /* NULL pointer, bad reduction, negative coefficient */
   FLCE_ERR_BAD_SHAPE = 2,     /* N, H or V out of the supported range */
-  FLCE_ERR_ALIGN = 3,         /* H or V not a multiple of 8, or a pointer not 16-byte aligned */
+  FLCE_ERR_ALIGN = 3,         /* H (or a [H,V] weight's V) not a multiple of 8, or a pointer
+                               * not 16-byte aligned */
   FLCE_ERR_WS_TOO_SMALL = 4,  /* ws_bytes < flce_workspace_size(...) */
   FLCE_ERR_LABEL = 5,         /* a label outside [0, V) that is not ignore_index */
   FLCE_ERR_TIMEOUT = 6,       /* a device pipeline wait exceeded its time limit */
   FLCE_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed */
   FLCE_ERR_DEVICE = 8,        /* current device is not an sm_103 GPU */
-  FLCE_ERR_SCRATCH_LIMIT = 9  /* problem needs more than FLCE_NOALLOC_SCRATCH_BYTES */
+  FLCE_ERR_SCRATCH_LIMIT = 9, /* problem needs more than FLCE_NOALLOC_SCRATCH_BYTES */
+  FLCE_ERR_BOUNDS = 10        /* libflce_debug.so only: an in-kernel bounds check failed
+                               * (the access was skipped; results are not valid) */
 };
 
 typedef struct {
@@ -110,7 +115,16 @@ typedef struct {
   /* flce_forward_backward's token chunk (a multiple of 512), 0 = auto: the largest
    * chunk whose fp32 logits and bf16 dlogits fit in 8 GiB. */
   int64_t chunk_n;
+  /* 0: dhidden is bf16 [N,H].  1: dhidden is fp32 [N,H] (32-byte aligned), the
+   * unrounded fp32 accumulation -- for a vocabulary shard's dhidden term, so that the
+   * sum over the shards is rounded once, after the exchange, not once per shard. */
+  int32_t dhidden_fp32;
 } flce_params;
+
+/* FLCE_OK, or the status every entry point returns for these parameters (checked
+ * on the host before any pointer is looked at): FLCE_ERR_BAD_ARG, FLCE_ERR_BAD_SHAPE
+ * or FLCE_ERR_ALIGN. */
+int flce_check_params(const flce_params* params);
 
 /* Bytes of device workspace that flce_forward / flce_shard_stats (phase 0),
  * flce_backward (phase 1), flce_combine_shards (phase 2) or flce_forward_backward
@@ -133,7 +147,8 @@ int flce_forward(const flce_params* params, const void* hidden, const void* weig
  *   lse, ez: the [N] outputs of flce_forward for the same inputs and params.
  *   g_loss, g_entropy: upstream gradients of loss and entropy, [N] for
  *     FLCE_RED_NONE, [1] otherwise; NULL means zero.
- *   dhidden [N,H] bf16, dweight [H,V] (or [V,H], as weight) bf16: overwritten.
+ *   dhidden [N,H] bf16 (fp32 with params->dhidden_fp32), dweight [H,V] (or [V,H], as
+ *   weight) bf16: overwritten.
  *   workspace: >= flce_workspace_size(params, 1) bytes, 256-byte aligned. */
 int flce_backward(const flce_params* params, const void* hidden, const void* weight,
                   const int64_t* labels, const float* lse, const float* ez,
@@ -191,7 +206,8 @@ int flce_combine_shards(const flce_params* params, const float* stats, int32_t n
 
 /* Synchronises `stream` and returns the device-side status recorded in the
  * workspace header by the last call that used this workspace (FLCE_OK,
- * FLCE_ERR_LABEL or FLCE_ERR_TIMEOUT), or FLCE_ERR_CUDA. */
+ * FLCE_ERR_LABEL, FLCE_ERR_TIMEOUT or, with libflce_debug.so, FLCE_ERR_BOUNDS), or
+ * FLCE_ERR_CUDA. */
 int flce_status(const void* workspace, void* stream);
 
 /* Number of kernels one call with these parameters enqueues (memsets not counted):

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG_DIR, "libflce.so")
 
 FLCE_OK = 0
 _ERR_NAMES = {1: "BAD_ARG", 2: "BAD_SHAPE", 3: "ALIGN", 4: "WS_TOO_SMALL", 5: "LABEL",
-              6: "TIMEOUT", 7: "CUDA", 8: "DEVICE", 9: "SCRATCH_LIMIT"}
+              6: "TIMEOUT", 7: "CUDA", 8: "DEVICE", 9: "SCRATCH_LIMIT", 10: "BOUNDS"}
 
 
 class FlceError(RuntimeError):
@@ -36,7 +36,8 @@ class FlceParams(ctypes.Structure):
                 ("validate", ctypes.c_int32), ("chunk_v", ctypes.c_int64),
                 ("weight_layout", ctypes.c_int32), ("label_smoothing", ctypes.c_float),
                 ("class_weight", ctypes.c_void_p), ("v_offset", ctypes.c_int64),
-                ("v_total", ctypes.c_int64), ("chunk_n", ctypes.c_int64)]
+                ("v_total", ctypes.c_int64), ("chunk_n", ctypes.c_int64),
+                ("dhidden_fp32", ctypes.c_int32)]
 
 
 WEIGHT_HV, WEIGHT_VH = 0, 1
@@ -57,7 +58,8 @@ _lock = threading.Lock()
 EXPORTED = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_status",
             "flce_kernel_launches", "flce_strerror", "flce_version", "flce_forward_noalloc",
             "flce_shard_stats", "flce_combine_shards", "flce_forward_backward",
-            "flce_scale_bf16", "flce_selftest_wait_timeout", "flce_plan_tiles")
+            "flce_scale_bf16", "flce_selftest_wait_timeout", "flce_plan_tiles",
+            "flce_check_params")
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -66,45 +68,70 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(path):
-            raise RuntimeError(
-                f"{path} is missing: build it with `python -m linear_cross_entropy_forward_gb300.build`")
-        lib = ctypes.CDLL(path)
-        P = ctypes.POINTER(FlceParams)
-        vp = ctypes.c_void_p
-        lib.flce_workspace_size.argtypes = [P, ctypes.c_int]
-        lib.flce_workspace_size.restype = ctypes.c_size_t
-        lib.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-        lib.flce_forward.restype = ctypes.c_int
-        lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
-                                      vp]
-        lib.flce_backward.restype = ctypes.c_int
-        lib.flce_status.argtypes = [vp, vp]
-        lib.flce_status.restype = ctypes.c_int
-        lib.flce_strerror.argtypes = [ctypes.c_int]
-        lib.flce_strerror.restype = ctypes.c_char_p
-        lib.flce_shard_stats.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-        lib.flce_shard_stats.restype = ctypes.c_int
-        lib.flce_combine_shards.argtypes = [P, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp,
-                                            ctypes.c_size_t, vp]
-        lib.flce_combine_shards.restype = ctypes.c_int
-        lib.flce_kernel_launches.argtypes = [P, ctypes.c_int]
-        lib.flce_kernel_launches.restype = ctypes.c_int
-        lib.flce_forward_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                              ctypes.c_size_t, vp]
-        lib.flce_forward_backward.restype = ctypes.c_int
-        lib.flce_scale_bf16.argtypes = [vp, ctypes.c_int64, vp, vp]
-        lib.flce_scale_bf16.restype = ctypes.c_int
-        lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint64, vp]
-        lib.flce_selftest_wait_timeout.restype = ctypes.c_int
-        i32 = ctypes.c_int32
-        lib.flce_plan_tiles.argtypes = [i32, i32, i32, ctypes.c_int64, i32, i32, i32,
-                                        ctypes.POINTER(i32)]
-        lib.flce_plan_tiles.restype = ctypes.c_int
-        lib.flce_version.argtypes = []
-        lib.flce_version.restype = ctypes.c_int
+        _lib = _open(path)
+        return _lib
+
+
+def use_library(path: str) -> ctypes.CDLL:
+    """Route every later call of this module through the library at `path` (the same
+    C ABI, e.g. libflce_debug.so, the build with in-kernel bounds checks); returns the
+    library used until now (None if none was loaded), to hand back later."""
+    global _lib
+    with _lock:
+        prev = _lib
+        _lib = _open(path)
+        return prev
+
+
+def restore_library(lib) -> None:
+    """Undo use_library: route calls through `lib` again (None: load on next use)."""
+    global _lib
+    with _lock:
         _lib = lib
-        return lib
+
+
+def _open(path: str) -> ctypes.CDLL:
+    """dlopen one build of the library and declare its signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m linear_cross_entropy_forward_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(FlceParams)
+    vp = ctypes.c_void_p
+    lib.flce_check_params.argtypes = [P]
+    lib.flce_check_params.restype = ctypes.c_int
+    lib.flce_workspace_size.argtypes = [P, ctypes.c_int]
+    lib.flce_workspace_size.restype = ctypes.c_size_t
+    lib.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.flce_forward.restype = ctypes.c_int
+    lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                  vp]
+    lib.flce_backward.restype = ctypes.c_int
+    lib.flce_status.argtypes = [vp, vp]
+    lib.flce_status.restype = ctypes.c_int
+    lib.flce_strerror.argtypes = [ctypes.c_int]
+    lib.flce_strerror.restype = ctypes.c_char_p
+    lib.flce_shard_stats.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.flce_shard_stats.restype = ctypes.c_int
+    lib.flce_combine_shards.argtypes = [P, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp,
+                                        ctypes.c_size_t, vp]
+    lib.flce_combine_shards.restype = ctypes.c_int
+    lib.flce_kernel_launches.argtypes = [P, ctypes.c_int]
+    lib.flce_kernel_launches.restype = ctypes.c_int
+    lib.flce_forward_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.c_size_t, vp]
+    lib.flce_forward_backward.restype = ctypes.c_int
+    lib.flce_scale_bf16.argtypes = [vp, ctypes.c_int64, vp, vp]
+    lib.flce_scale_bf16.restype = ctypes.c_int
+    lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint64, vp]
+    lib.flce_selftest_wait_timeout.restype = ctypes.c_int
+    i32 = ctypes.c_int32
+    lib.flce_plan_tiles.argtypes = [i32, i32, i32, ctypes.c_int64, i32, i32, i32,
+                                    ctypes.POINTER(i32)]
+    lib.flce_plan_tiles.restype = ctypes.c_int
+    lib.flce_version.argtypes = []
+    lib.flce_version.restype = ctypes.c_int
+    return lib
 
 
 def _check(code: int):
@@ -115,16 +142,17 @@ def _check(code: int):
 def make_params(N, H, V, reduction="mean", ignore_index=IGNORE_INDEX, zloss_coef=0.0,
                 softcap=0.0, validate=False, chunk_v=0, weight_layout="hv",
                 label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0,
-                chunk_n=0) -> FlceParams:
+                chunk_n=0, dhidden_fp32=False) -> FlceParams:
     """class_weight: a CUDA fp32 [V] tensor (kept alive by the caller) or None.
     v_offset / v_total: this weight is columns [v_offset, v_offset + V) of a vocabulary
     of v_total entries (0: the whole vocabulary).  chunk_n: token chunk of
-    flce_forward_backward (multiple of 512, 0 = auto)."""
+    flce_forward_backward (multiple of 512, 0 = auto).  dhidden_fp32: the backward
+    writes dhidden as fp32 (unrounded) instead of bf16."""
     cw = class_weight.data_ptr() if class_weight is not None else None
     return FlceParams(int(N), int(H), int(V), int(ignore_index), reduction_code(reduction),
                       float(zloss_coef), float(softcap), 1 if validate else 0, int(chunk_v),
                       layout_code(weight_layout), float(label_smoothing), cw, int(v_offset),
-                      int(v_total), int(chunk_n))
+                      int(v_total), int(chunk_n), 1 if dhidden_fp32 else 0)
 
 
 def _dims(hidden, weight, weight_layout):
@@ -135,9 +163,11 @@ def _dims(hidden, weight, weight_layout):
 
 
 def workspace_size(params: FlceParams, phase: int) -> int:
-    n = load_library().flce_workspace_size(ctypes.byref(params), phase)
+    lib = load_library()
+    _check(lib.flce_check_params(ctypes.byref(params)))
+    n = lib.flce_workspace_size(ctypes.byref(params), phase)
     if n == 0:
-        raise FlceError(1, "invalid parameters for workspace sizing")
+        raise FlceError(1, f"no workspace phase {phase}")
     return int(n)
 
 
@@ -245,9 +275,10 @@ def flce_forward(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_I
 def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction="mean",
                   ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0, validate=False,
                   chunk_v=0, workspace=None, stream=None, out=None, weight_layout="hv",
-                  label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0):
-    """Backward pass through the C ABI; returns (dhidden [N,H] bf16, dweight bf16 shaped
-    like weight).
+                  label_smoothing=0.0, class_weight=None, v_offset=0, v_total=0,
+                  dhidden_fp32=False):
+    """Backward pass through the C ABI; returns (dhidden [N,H] bf16 -- fp32 with
+    dhidden_fp32 --, dweight bf16 shaped like weight).
 
     g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
     With a vocabulary shard (v_total > 0) dweight is the shard's and dhidden is the
@@ -264,18 +295,20 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
     if class_weight is not None:
         _need(class_weight, "class_weight", torch.float32, (V,), dev)
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate, chunk_v,
-                    weight_layout, label_smoothing, class_weight, v_offset, v_total)
+                    weight_layout, label_smoothing, class_weight, v_offset, v_total,
+                    dhidden_fp32=dhidden_fp32)
     n_g = N if p.reduction == RED_NONE else 1
     if g_loss is not None:
         _need(g_loss, "g_loss", torch.float32, (n_g,), dev)
     if g_entropy is not None:
         _need(g_entropy, "g_entropy", torch.float32, (n_g,), dev)
+    dh_dtype = torch.float32 if dhidden_fp32 else torch.bfloat16
     if out is None:
-        dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dh = torch.empty(N, H, dtype=dh_dtype, device=dev)
         dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
     else:
-        bf = torch.bfloat16
-        dh, dw = _need_out(out, [("dhidden", (N, H), bf), ("dweight", wshape, bf)], dev)
+        dh, dw = _need_out(out, [("dhidden", (N, H), dh_dtype),
+                                 ("dweight", wshape, torch.bfloat16)], dev)
     ws = _workspace(p, 1, dev, workspace)
     _check(lib.flce_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                              _ptr(lse), _ptr(ez), _ptr(g_loss), _ptr(g_entropy), _ptr(dh),
@@ -286,12 +319,14 @@ def flce_backward(hidden, weight, labels, lse, ez, g_loss, g_entropy, reduction=
 def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
                           ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0,
                           validate=False, chunk_n=0, workspace=None, stream=None, out=None,
-                          weight_layout="hv", label_smoothing=0.0, class_weight=None):
+                          weight_layout="hv", label_smoothing=0.0, class_weight=None,
+                          dhidden_fp32=False):
     """Forward and backward in one call (the upstream gradients known up front).
 
     g_loss / g_entropy: fp32 [N] for reduction 'none', [1] otherwise, or None (zero).
     Returns (loss, entropy, lse, ez, dhidden, dweight) -- what flce_forward followed by
-    flce_backward returns -- at 6*N*H*V flops instead of 8*N*H*V.
+    flce_backward returns -- at 6*N*H*V flops instead of 8*N*H*V.  dhidden is fp32
+    with dhidden_fp32.
     """
     lib = load_library()
     N, H, V, wshape = _dims(hidden, weight, weight_layout)
@@ -303,8 +338,9 @@ def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="
         _need(class_weight, "class_weight", torch.float32, (V,), dev)
     p = make_params(N, H, V, reduction, ignore_index, zloss_coef, softcap, validate,
                     weight_layout=weight_layout, label_smoothing=label_smoothing,
-                    class_weight=class_weight, chunk_n=chunk_n)
+                    class_weight=class_weight, chunk_n=chunk_n, dhidden_fp32=dhidden_fp32)
     n_g = N if p.reduction == RED_NONE else 1
+    dh_dtype = torch.float32 if dhidden_fp32 else torch.bfloat16
     if g_loss is not None:
         _need(g_loss, "g_loss", torch.float32, (n_g,), dev)
     if g_entropy is not None:
@@ -314,13 +350,14 @@ def flce_forward_backward(hidden, weight, labels, g_loss, g_entropy, reduction="
         ent = torch.empty(n_g, dtype=torch.float32, device=dev)
         lse = torch.empty(N, dtype=torch.float32, device=dev)
         ez = torch.empty(N, dtype=torch.float32, device=dev)
-        dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dh = torch.empty(N, H, dtype=dh_dtype, device=dev)
         dw = torch.empty(wshape, dtype=torch.bfloat16, device=dev)
     else:
         f32, bf = torch.float32, torch.bfloat16
         loss, ent, lse, ez, dh, dw = _need_out(
             out, [("loss", (n_g,), f32), ("entropy", (n_g,), f32), ("lse", (N,), f32),
-                  ("ez", (N,), f32), ("dhidden", (N, H), bf), ("dweight", wshape, bf)], dev)
+                  ("ez", (N,), f32), ("dhidden", (N, H), dh_dtype),
+                  ("dweight", wshape, bf)], dev)
     ws = _workspace(p, 3, dev, workspace)
     _check(lib.flce_forward_backward(ctypes.byref(p), _ptr(hidden), _ptr(weight), _ptr(labels),
                                      _ptr(g_loss), _ptr(g_entropy), _ptr(loss), _ptr(ent),

@@ -5,7 +5,11 @@ into ``libflce.so`` next to this file with the CUDA runtime linked statically,
 so the library loads on a machine without a GPU (the C-ABI symbol test) and
 needs only the driver on a GPU machine.
 
-    python -m linear_cross_entropy_forward_gb300.build [--verbose-ptxas] [--force]
+``--debug`` builds ``libflce_debug.so`` instead: the same sources with FLCE_DEBUG=1,
+which compiles in-kernel bounds checks of every TMA box and epilogue store (a
+failing check is reported as FLCE_ERR_BOUNDS and the access skipped).
+
+    python -m linear_cross_entropy_forward_gb300.build [--verbose-ptxas] [--force] [--debug]
 """
 from __future__ import annotations
 
@@ -21,6 +25,8 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libflce.so")
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libflce_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,26 +51,32 @@ def _deps():
     return deps
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _up_to_date(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) -> str:
-    """Compile every CUDA source for sm_103a and link libflce.so; returns its path."""
-    if not force and not verbose_ptxas and _up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True,
+          debug: bool = False) -> str:
+    """Compile every CUDA source for sm_103a and link libflce.so (libflce_debug.so, with
+    the in-kernel bounds checks, when debug is set); returns its path."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and not verbose_ptxas and _up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                     "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
+    if debug:
+        flags += ["-DFLCE_DEBUG=1"]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -77,23 +89,25 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
         for _, log in results:
             sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if not quiet:
-        print(f"built {LIB_PATH}")
-    return LIB_PATH
+        print(f"built {lib_path}")
+    return lib_path
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose-ptxas", action="store_true")
+    ap.add_argument("--debug", action="store_true",
+                    help="build libflce_debug.so (in-kernel bounds checks)")
     a = ap.parse_args()
-    build(force=a.force, verbose_ptxas=a.verbose_ptxas, quiet=False)
+    build(force=a.force, verbose_ptxas=a.verbose_ptxas, quiet=False, debug=a.debug)
 
 
 if __name__ == "__main__":

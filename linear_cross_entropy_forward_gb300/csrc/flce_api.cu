@@ -55,6 +55,13 @@ struct FwdLayout {
 };
 
 constexpr size_t kWsumOffset = 64;  // float in the workspace header: sum of class weights
+// two uint32 counters of the GEMMs' dynamic tile schedule in the workspace header
+// (zeroed with the header at the start of every call, and by each GEMM at its end)
+constexpr size_t kSchedOffset = 128;
+
+inline unsigned int* sched_counters(uint32_t* header) {
+  return reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(header) + kSchedOffset);
+}
 
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
@@ -102,7 +109,9 @@ BwdLayout bwd_layout(const flce_params* p) {
   if (p->label_smoothing != 0.0f) off += align256(static_cast<size_t>(p->N) * 4);
   L.dl = off; off += align256(static_cast<size_t>(p->N) * L.Vc * 2);
   L.acc = off;
-  if (L.chunks > 1) off += align256(static_cast<size_t>(p->N) * p->H * 4);
+  // several chunks accumulate dhidden in fp32: here, unless the caller's fp32 dhidden
+  // is the accumulator itself
+  if (L.chunks > 1 && !p->dhidden_fp32) off += align256(static_cast<size_t>(p->N) * p->H * 4);
   L.total = off;
   return L;
 }
@@ -158,9 +167,13 @@ int check_params(const flce_params* p) {
   if (!(p->zloss_coef >= 0.0f) || !(p->softcap >= 0.0f)) return FLCE_ERR_BAD_ARG;
   if (p->N < 0 || p->H < 8 || p->V < 1) return FLCE_ERR_BAD_SHAPE;
   if (p->N > kMaxDim || p->H > kMaxDim || p->V > kMaxDim) return FLCE_ERR_BAD_SHAPE;
-  if (p->H % 8 != 0 || p->V % 8 != 0) return FLCE_ERR_ALIGN;
+  // row strides of the TMA engine are multiples of 16 bytes: H always (hidden, a [V,H]
+  // weight), V only where it is a row length (a [H,V] weight and its dweight)
+  if (p->H % 8 != 0) return FLCE_ERR_ALIGN;
+  if (p->weight_layout == FLCE_WEIGHT_HV && p->V % 8 != 0) return FLCE_ERR_ALIGN;
   if (p->chunk_v < 0 || (p->chunk_v > 0 && p->chunk_v % 256 != 0)) return FLCE_ERR_BAD_ARG;
   if (p->chunk_n < 0 || p->chunk_n % 512 != 0) return FLCE_ERR_BAD_ARG;
+  if (p->dhidden_fp32 != 0 && p->dhidden_fp32 != 1) return FLCE_ERR_BAD_ARG;
   if (p->weight_layout != FLCE_WEIGHT_HV && p->weight_layout != FLCE_WEIGHT_VH)
     return FLCE_ERR_BAD_ARG;
   if (!(p->label_smoothing >= 0.0f && p->label_smoothing <= 1.0f)) return FLCE_ERR_BAD_ARG;
@@ -177,6 +190,11 @@ int check_params(const flce_params* p) {
 }
 
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+// dhidden: bf16 needs 16-byte alignment; fp32 is the accumulator of the 256-bit
+// accesses of the dhidden epilogue and needs 32
+inline bool dhidden_aligned(const flce_params* p, const void* ptr) {
+  return (reinterpret_cast<uintptr_t>(ptr) & (p->dhidden_fp32 ? 31 : 15)) == 0;
+}
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point, so the library
 // links no libcuda at build time.
@@ -205,20 +223,37 @@ EncodeTiledFn get_encode_fn() {
 #define FLCE_L2_PROMOTION 3
 #endif
 
-// 2-D bf16 tensor map over a row-major [outer, inner] array with a {box_inner, box_outer}
+// A 2-D bf16 tensor map and the extents of the array it covers (the FLCE_DEBUG
+// build checks every TMA box of a GEMM against them).
+struct Map {
+  CUtensorMap m;
+  int64_t inner = 0, outer = 0;
+};
+
+// Tensor map over a row-major [outer, inner] bf16 array with a {box_inner, box_outer}
 // box, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
-              int64_t row_elems, int box_inner, int box_outer) {
+bool make_map(Map* map, const void* base, int64_t inner, int64_t outer, int64_t row_elems,
+              int box_inner, int box_outer) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
+  map->inner = inner;
+  map->outer = outer;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(&map->m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              static_cast<CUtensorMapL2promotion>(FLCE_L2_PROMOTION),
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The GEMM's A and B operand extents, from their maps.
+void set_extents(GemmShape* sh, const Map& a, const Map& b) {
+  sh->a_inner = a.inner;
+  sh->a_outer = a.outer;
+  sh->b_inner = b.inner;
+  sh->b_outer = b.outer;
 }
 
 struct DevInfo {
@@ -251,6 +286,7 @@ int read_status(const void* workspace, cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
   if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return FLCE_ERR_CUDA;
+  if (word & FLCE_DEVERR_BOUNDS) return FLCE_ERR_BOUNDS;
   if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
   if (word & FLCE_DEVERR_LABEL) return FLCE_ERR_LABEL;
   return FLCE_OK;
@@ -327,17 +363,23 @@ const char* flce_strerror(int code) {
     case FLCE_OK: return "ok";
     case FLCE_ERR_BAD_ARG: return "invalid argument";
     case FLCE_ERR_BAD_SHAPE: return "unsupported shape (need N >= 0, H >= 8, V >= 1)";
-    case FLCE_ERR_ALIGN: return "H and V must be multiples of 8 and pointers 16-byte aligned";
+    case FLCE_ERR_ALIGN:
+      return "H (and V of a [H,V] weight) must be multiples of 8 and pointers 16-byte aligned "
+             "(fp32 dhidden: 32)";
     case FLCE_ERR_WS_TOO_SMALL: return "workspace smaller than flce_workspace_size()";
     case FLCE_ERR_LABEL: return "label outside [0, V) that is not ignore_index";
     case FLCE_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FLCE_ERR_CUDA: return "CUDA call failed";
     case FLCE_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case FLCE_ERR_BOUNDS:
+      return "a device-side bounds check of the FLCE_DEBUG build failed (access skipped)";
     case FLCE_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than flce_forward_noalloc's static 64 MiB array";
     default: return "unknown status";
   }
 }
+
+int flce_check_params(const flce_params* p) { return check_params(p); }
 
 size_t flce_workspace_size(const flce_params* p, int phase) {
   if (check_params(p) != FLCE_OK) return 0;
@@ -399,7 +441,7 @@ namespace {
 // raw fp32 logits [rows, ld_z].
 struct StatsOut {
   float *pm, *pd, *ps, *psw, *zlabel, *zout;
-  int64_t part_stride, ld_z;
+  int64_t part_stride, ld_z, n_parts;
 };
 
 // Logits tiles of hidden rows [n0, n0 + rows) @ weight reduced to online-softmax
@@ -409,7 +451,7 @@ int launch_stats(const flce_params* p, const void* hidden, const void* weight,
                  uint32_t* err, cudaStream_t st) {
   const int64_t N = p->N, H = p->H, V = p->V;
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
-  CUtensorMap tmA, tmB;
+  Map tmA, tmB;
   if (!make_map(&tmA, hidden, H, N, H, BK, 64)) return FLCE_ERR_CUDA;
   // weight as B: [H,V] is MN-major, [V,H] K-major ({64,64} boxes either way)
   if (!(vh ? make_map(&tmB, weight, H, V, H, BK, 64)
@@ -422,6 +464,7 @@ int launch_stats(const flce_params* p, const void* hidden, const void* weight,
   sh.k_blocks = static_cast<int>(cdiv(H, BK));
   sh.a_mn_off = static_cast<int>(n0);
   sh.raster = 0;
+  sh.sched = sched_counters(err);
   plan_tiles(&sh, int64_t(PAIR_BM) * H * 2);
   EpiArgs ea{};
   ea.rows = static_cast<int>(rows);
@@ -443,7 +486,9 @@ int launch_stats(const flce_params* p, const void* hidden, const void* weight,
   ea.zout = o.zout;
   ea.ld_z = o.ld_z;
   ea.err = err;
-  return cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA, tmB, sh, ea, st));
+  ea.n_parts = o.n_parts;
+  set_extents(&sh, tmA, tmB);
+  return cuda_rc((vh ? launch_fwd_stats_vh : launch_fwd_stats)(tmA.m, tmB.m, sh, ea, st));
 }
 
 // Stage 1 of the forward over all rows, into the forward workspace layout.
@@ -457,6 +502,7 @@ int run_fwd_stats(const flce_params* p, const void* hidden, const void* weight,
   o.psw = reinterpret_cast<float*>(ws + L.psw);
   o.zlabel = reinterpret_cast<float*>(ws + L.zlabel);
   o.part_stride = p->N;
+  o.n_parts = L.n_parts;
   *out = o;
   return launch_stats(p, hidden, weight, labels, 0, p->N, o, err, st);
 }
@@ -607,7 +653,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   if (!weight || !dweight || !workspace) return FLCE_ERR_BAD_ARG;
   if (p->N > 0 && (!hidden || !labels || !lse || !ez || !dhidden)) return FLCE_ERR_BAD_ARG;
   if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(lse) ||
-      !aligned16(ez) || !aligned16(dhidden) || !aligned16(dweight) ||
+      !aligned16(ez) || !dhidden_aligned(p, dhidden) || !aligned16(dweight) ||
       (reinterpret_cast<uintptr_t>(g_loss) & 3) || (reinterpret_cast<uintptr_t>(g_entropy) & 3) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255))
     return FLCE_ERR_ALIGN;
@@ -643,7 +689,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
   // dlogits chunk: MN-major (dweight) and K-major (dhidden); weight: as the
   // recompute's B and as dhidden's B, each K- or MN-major depending on its layout.
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
-  CUtensorMap mHidK, mHidMn, mDlMn, mDlK, mWRec, mWDh;
+  Map mHidK, mHidMn, mDlMn, mDlK, mWRec, mWDh;
   bool ok = make_map(&mHidK, hidden, H, N, H, BK, 64) &&
             make_map(&mHidMn, hidden, H, N, H, 64, BK) &&
             make_map(&mDlMn, dl, L.Vc, N, L.Vc, 64, BK) &&
@@ -666,6 +712,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s3.n_tiles = static_cast<int>(cdiv(w, TN_DLOGITS));
     s3.k_blocks = static_cast<int>(cdiv(H, BK));
     s3.raster = 0;
+    s3.sched = sched_counters(err);
     plan_tiles(&s3, int64_t(PAIR_BM) * H * 2);
     s3.b_mn_off = static_cast<int>(v0);
     EpiArgs e3{};
@@ -684,7 +731,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     e3.dl = dl;
     e3.ld_dl = L.Vc;
     e3.err = err;
-    if ((rc = cuda_rc((vh ? launch_bwd_dlogits_vh : launch_bwd_dlogits)(mHidK, mWRec, s3, e3,
+    set_extents(&s3, mHidK, mWRec);
+    if ((rc = cuda_rc((vh ? launch_bwd_dlogits_vh : launch_bwd_dlogits)(mHidK.m, mWRec.m, s3, e3,
                                                                         st))))
       return rc;
 
@@ -693,6 +741,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     // (rows v, hidden revisited as B).  Both operands are MN-major views.
     GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
+    s4.sched = sched_counters(err);
     EpiArgs e4{};
     e4.V = V;
     e4.err = err;
@@ -717,8 +766,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       e4.out = static_cast<__nv_bfloat16*>(dweight);
       e4.ld_out = V;
     }
-    if ((rc = cuda_rc(vh ? launch_bwd_dweight(mDlMn, mHidMn, s4, e4, st)
-                         : launch_bwd_dweight(mHidMn, mDlMn, s4, e4, st))))
+    set_extents(&s4, vh ? mDlMn : mHidMn, vh ? mHidMn : mDlMn);
+    if ((rc = cuda_rc(vh ? launch_bwd_dweight(mDlMn.m, mHidMn.m, s4, e4, st)
+                         : launch_bwd_dweight(mHidMn.m, mDlMn.m, s4, e4, st))))
       return rc;
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
@@ -728,21 +778,30 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(w, BK));
     s5.raster = 1;
+    s5.sched = sched_counters(err);
     plan_tiles(&s5, int64_t(TN_DHIDDEN) * w * 2);
     s5.b_k_off = static_cast<int>(v0);
     EpiArgs e5{};
     e5.rows = static_cast<int>(N);
     e5.cols = static_cast<int>(H);
     e5.V = V;
-    e5.acc = acc;
-    e5.acc_out = static_cast<__nv_bfloat16*>(dhidden);
     e5.ld_acc = H;
-    e5.acc_mode = L.chunks == 1 ? ACC_ONLY
-                  : c == 0      ? ACC_FIRST
-                  : c == L.chunks - 1 ? ACC_LAST
-                                      : ACC_MID;
+    if (p->dhidden_fp32) {
+      // the caller's fp32 dhidden is the accumulator: stored by the first chunk,
+      // added to by the others, never rounded
+      e5.acc = static_cast<float*>(dhidden);
+      e5.acc_mode = c == 0 ? ACC_FIRST : ACC_MID;
+    } else {
+      e5.acc = acc;
+      e5.acc_out = static_cast<__nv_bfloat16*>(dhidden);
+      e5.acc_mode = L.chunks == 1 ? ACC_ONLY
+                    : c == 0      ? ACC_FIRST
+                    : c == L.chunks - 1 ? ACC_LAST
+                                        : ACC_MID;
+    }
     e5.err = err;
-    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK, mWDh, s5, e5,
+    set_extents(&s5, mDlK, mWDh);
+    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK.m, mWDh.m, s5, e5,
                                                                         st))))
       return rc;
   }
@@ -761,7 +820,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
   if (!loss || !entropy || !workspace || !weight || !dweight) return FLCE_ERR_BAD_ARG;
   if (p->N > 0 && (!hidden || !labels || !lse || !ez || !dhidden)) return FLCE_ERR_BAD_ARG;
   if (!aligned16(hidden) || !aligned16(weight) || !aligned16(labels) || !aligned16(loss) ||
-      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) || !aligned16(dhidden) ||
+      !aligned16(entropy) || !aligned16(lse) || !aligned16(ez) || !dhidden_aligned(p, dhidden) ||
       !aligned16(dweight) || (reinterpret_cast<uintptr_t>(g_loss) & 3) ||
       (reinterpret_cast<uintptr_t>(g_entropy) & 3) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -798,6 +857,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
   so.zout = reinterpret_cast<float*>(ws + L.z);
   so.part_stride = L.Nc;
   so.ld_z = L.ldz;
+  so.n_parts = L.n_parts;
   float* loss_row = per_token ? loss : reinterpret_cast<float*>(ws + L.loss_row);
   float* ent_row = per_token ? entropy : reinterpret_cast<float*>(ws + L.ent_row);
   float4* rowc = reinterpret_cast<float4*>(ws + L.rowc);
@@ -806,7 +866,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
   float* dwacc = reinterpret_cast<float*>(ws + L.dwacc);
 
   // hidden as dweight's operand (MN-major, tokens along K); weight as dhidden's B
-  CUtensorMap mHidMn, mWDh;
+  Map mHidMn, mWDh;
   bool ok = make_map(&mHidMn, hidden, H, N, H, 64, BK);
   ok = ok && (vh ? make_map(&mWDh, weight, H, V, H, 64, BK)
                  : make_map(&mWDh, weight, V, H, V, BK, 64));
@@ -831,8 +891,9 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
         p->class_weight, rowc, rowd);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
     {
+      const int64_t row_steps = cdiv(rows, kDlzRows);
       const dim3 grid(static_cast<unsigned>(cdiv(L.ldz, kDlzCols)),
-                      static_cast<unsigned>(rows < 65535 ? rows : 65535));
+                      static_cast<unsigned>(row_steps < 65535 ? row_steps : 65535));
       dlogits_from_z_kernel<<<grid, kDlzThreads, 0, st>>>(
           so.zout, rows, L.ldz, rowc, rowd, lab, V, p->softcap, smooth ? 1 : 0,
           p->class_weight, dl);
@@ -840,7 +901,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     }
 
     // the chunk's dlogits [rows, V]: rows past `rows` read as zeros
-    CUtensorMap mDlK, mDlMn;
+    Map mDlK, mDlMn;
     ok = make_map(&mDlK, dl, V, rows, L.ldz, BK, 64) &&
          make_map(&mDlMn, dl, V, rows, L.ldz, 64, BK);
     if (!ok) return FLCE_ERR_CUDA;
@@ -853,22 +914,30 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     s5.n_tiles = static_cast<int>(cdiv(H, TN_DHIDDEN));
     s5.k_blocks = static_cast<int>(cdiv(V, BK));
     s5.raster = 0;
+    s5.sched = sched_counters(err);
     plan_tiles(&s5, int64_t(PAIR_BM) * V * 2);
     EpiArgs e5{};
     e5.rows = static_cast<int>(rows);
     e5.cols = static_cast<int>(H);
     e5.V = V;
-    e5.acc_out = static_cast<__nv_bfloat16*>(dhidden) + n0 * H;
     e5.ld_acc = H;
-    e5.acc_mode = ACC_ONLY;
+    if (p->dhidden_fp32) {
+      e5.acc = static_cast<float*>(dhidden) + n0 * H;  // 32-byte aligned: H % 8 == 0
+      e5.acc_mode = ACC_FIRST;
+    } else {
+      e5.acc_out = static_cast<__nv_bfloat16*>(dhidden) + n0 * H;
+      e5.acc_mode = ACC_ONLY;
+    }
     e5.err = err;
-    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK, mWDh, s5, e5,
+    set_extents(&s5, mDlK, mWDh);
+    if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK.m, mWDh.m, s5, e5,
                                                                         st))))
       return rc;
 
     // dweight (+)= hidden[n0 : n0 + rows]^T @ dlogits ([H,V]) or its transpose ([V,H])
     GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.k_blocks = static_cast<int>(cdiv(rows, BK));
+    s4.sched = sched_counters(err);
     EpiArgs e4{};
     e4.V = V;
     e4.err = err;
@@ -891,18 +960,19 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
       e4.cols = static_cast<int>(V);
     }
     const int64_t ld_dw = vh ? H : V;
-    const CUtensorMap& a4 = vh ? mDlMn : mHidMn;
-    const CUtensorMap& b4 = vh ? mHidMn : mDlMn;
+    const Map& a4 = vh ? mDlMn : mHidMn;
+    const Map& b4 = vh ? mHidMn : mDlMn;
+    set_extents(&s4, a4, b4);
     if (L.chunks == 1) {
       e4.out = static_cast<__nv_bfloat16*>(dweight);
       e4.ld_out = ld_dw;
-      rc = cuda_rc(launch_bwd_dweight(a4, b4, s4, e4, st));
+      rc = cuda_rc(launch_bwd_dweight(a4.m, b4.m, s4, e4, st));
     } else {
       e4.acc = dwacc;
       e4.acc_out = static_cast<__nv_bfloat16*>(dweight);
       e4.ld_acc = ld_dw;
       e4.acc_mode = c == 0 ? ACC_FIRST : c == L.chunks - 1 ? ACC_LAST : ACC_MID;
-      rc = cuda_rc(launch_bwd_dweight_acc(a4, b4, s4, e4, st));
+      rc = cuda_rc(launch_bwd_dweight_acc(a4.m, b4.m, s4, e4, st));
     }
     if (rc) return rc;
   }

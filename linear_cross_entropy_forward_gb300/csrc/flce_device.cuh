@@ -30,6 +30,7 @@ namespace flce {
 enum : uint32_t {
   FLCE_DEVERR_TIMEOUT = 1u,
   FLCE_DEVERR_LABEL = 2u,
+  FLCE_DEVERR_BOUNDS = 4u,  // an in-kernel bounds check of the FLCE_DEBUG build failed
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -142,6 +143,32 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+// Arrive without release semantics on a barrier of any CTA of the cluster: it orders
+// none of this thread's earlier memory operations.  A release arrive on the thread
+// that issues the UMMAs waited for its tensor operations in flight and drained the
+// pipe (measured), so that thread acknowledges with this one, after an acquire load.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// 32-bit shared-memory load with acquire semantics: no later memory operation of this
+// thread (a relaxed arrive that hands the slot back, say) is performed before it.
+__device__ __forceinline__ int ld_acquire_shared(const volatile int* p) {
+  int v;
+  asm volatile("ld.acquire.cluster.shared::cta.b32 %0, [%1];"
+               : "=r"(v)
+               : "r"(smem_u32(const_cast<const int*>(p)))
+               : "memory");
+  return v;
+}
+// Arrive on a barrier of this CTA (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// 32-bit store to a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // Tile load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (shared::cluster address),
@@ -321,6 +348,38 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// Three-input maximum / minimum (sm_100-class SMs): one instruction for two steps
+// of a reduction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Maximum / minimum of 32 values in 16 instructions, as a tree (5 levels deep).
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fmaxf(x[30], x[31]);
+  const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]);
+  const float b2 = fmax3(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return fmaxf(fmax3(b0, b1, b2), b3);
+}
+__device__ __forceinline__ float min32(const float (&x)[32]) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = fmin3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fminf(x[30], x[31]);
+  const float b0 = fmin3(a[0], a[1], a[2]), b1 = fmin3(a[3], a[4], a[5]);
+  const float b2 = fmin3(a[6], a[7], a[8]), b3 = fminf(a[9], a[10]);
+  return fminf(fmin3(b0, b1, b2), b3);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

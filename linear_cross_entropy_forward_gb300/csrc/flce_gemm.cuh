@@ -30,6 +30,17 @@
 // A cluster is exactly one pair, and every TMA load lands in the shared memory of
 // the CTA that issues it: no tile is delivered to more than one CTA.
 //
+// Tiles are handed out dynamically: each pair takes its first tile by its cluster
+// index and every later one from a global counter in the workspace header, so the
+// tiles in flight stay a window of consecutive tiles of the raster order however
+// unevenly the pairs progress (a static round-robin let them drift apart by many
+// tiles over a long schedule, and the operand panels they shared fell out of L2).
+// The peer CTA's warp 1 (idle otherwise: the leader issues the pair's UMMAs) is the
+// pair's scheduler: it draws the tiles and publishes them through a two-slot ring in
+// shared memory to every role of both CTAs, so no role on the pipeline's critical
+// path waits for a global atomic.  The last pair to finish resets the counter for the
+// next launch.
+//
 // Operands arrive as 64-row pieces of 8 KB ({64 K, 64 rows} boxes for K-major,
 // {64 MN, 64 K} boxes of the transposed view for MN-major); operand majorness is a
 // template choice, so no transposed copy of any tensor is made.  Every barrier
@@ -38,6 +49,7 @@
 
 #include <atomic>
 
+#include "flce_check.cuh"
 #include "flce_device.cuh"
 
 namespace flce {
@@ -64,6 +76,10 @@ __host__ __device__ constexpr int pair_threads() {
   return 64 + 32 * epi_warps<EPI>();
 }
 constexpr int TMEM_COLS = 512;
+// Depth of the ring that publishes each pair's tiles: the scheduler runs at most this
+// many tiles (plus the one it has drawn) ahead of the slowest role of the pair, which
+// keeps the tiles in flight across the GPU close together in the raster order.
+constexpr int TILE_RING = 2;
 constexpr uint32_t MN_ATOM_BYTES = 64 * BK * 2;  // one {64 MN x 64 K} box
 constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
 
@@ -89,7 +105,8 @@ struct PairCfg {
   static constexpr int STAGES = STAGES_FIT > FLCE_MAX_STAGES ? FLCE_MAX_STAGES : STAGES_FIT;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
-  static_assert((2 * STAGES + 2 * NACC) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 2 * NACC + 2 * TILE_RING) * 8 + 8 + 4 * TILE_RING <= BAR_BYTES,
+                "barrier area");
 };
 
 // Tile width (UMMA N) of each kernel of the path.
@@ -120,6 +137,13 @@ struct GemmShape {
   int b_mn_off, b_k_off;      // added to B's (mn, k) tile coordinates
   uint32_t mn_lbo, mn_sbo;    // descriptor strides of MN-major operands (bytes)
   int a_hint, b_hint;         // L2 eviction priority of A / B tile loads (L2Hint)
+  // dynamic schedule: sched[0] counts the tiles drawn after each pair's first,
+  // sched[1] the pairs that finished; both zero at launch, and zero again when the
+  // kernel ends (the last pair to finish resets them)
+  unsigned int* sched;
+  // extents (inner, outer) of the arrays behind the A and B tensor maps: the
+  // FLCE_DEBUG build checks every TMA box against them
+  int64_t a_inner, a_outer, b_inner, b_outer;
 };
 
 struct EpiArgs {
@@ -158,7 +182,20 @@ struct EpiArgs {
   int64_t ld_acc;
   int acc_mode;
   uint32_t* err;
+  int64_t n_parts;      // EPI_FWD_STATS: column parts of pm / pd / ps (bounds checks)
 };
+
+// A bounds check of the FLCE_DEBUG build: true in the regular build; in the debug
+// build a failing check records FLCE_DEVERR_BOUNDS and the caller skips the access.
+#if FLCE_DEBUG
+__device__ __forceinline__ bool debug_ok(bool ok, uint32_t* err) {
+  if (!ok && err) atomicOr(err, FLCE_DEVERR_BOUNDS);
+  return ok;
+}
+#define FLCE_CHECK(cond, err) ::flce::debug_ok((cond), (err))
+#else
+#define FLCE_CHECK(cond, err) true
+#endif
 
 // Tile order of the persistent schedule.  raster 0: groups of `group` consecutive
 // m-tiles, m fastest within a group, every n-tile of the group before the next
@@ -188,18 +225,24 @@ constexpr uint32_t PIECE_BYTES = 64 * BK * 2;  // 64 rows (MN) x 64 (K), either 
 
 // One stage of an operand: ROWS (MN) x 64 (K) as ROWS/64 pieces of 64 rows, 8 KB
 // apart (K-major: {64, 64} boxes; MN-major: {64, 64} boxes of the transposed view),
-// all loaded into this CTA's own shared memory.
+// all loaded into this CTA's own shared memory.  The FLCE_DEBUG build checks each box
+// against the array's extents (inner, outer) first and returns false, loading
+// nothing more, at the first one out of range.
 template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint32_t fb,
-                                             int mn0, int k0, uint64_t pol) {
+__device__ __forceinline__ bool load_operand(uint8_t* dst, const CUtensorMap* map, uint32_t fb,
+                                             int mn0, int k0, uint64_t pol, int64_t inner,
+                                             int64_t outer) {
   static_assert(ROWS % 64 == 0, "operand rows");
 #pragma unroll
   for (int j = 0; j < ROWS / 64; ++j) {
-    if constexpr (MN)
-      tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, mn0 + 64 * j, k0, pol);
-    else
-      tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, k0, mn0 + 64 * j, pol);
+    const int x = MN ? mn0 + 64 * j : k0;
+    const int y = MN ? k0 : mn0 + 64 * j;
+#if FLCE_DEBUG
+    if (!tma_box_ok(x, y, inner, outer)) return false;
+#endif
+    tma_load_2d_pair_hint(dst + j * PIECE_BYTES, map, fb, x, y, pol);
   }
+  return true;
 }
 
 template <bool MN>
@@ -220,7 +263,13 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, const Ge
 template <int EPI>
 struct Epilogue;
 
-// Online-softmax partial statistics of one row over its CH*32 columns.
+// Online-softmax partial statistics of one row over its CH*32 columns, in log2
+// units: u = log2e * z for the (capped) logit z, m = max u, d = sum 2^{u - m},
+// s = sum 2^{u - m} (u - m).  Each 32-column chunk takes its maximum before any
+// exponential: without the cap over the raw accumulators x (u = log2e x is monotone
+// in x, so max u = log2e max x exactly); with it over r = 1 / (1 + 2^{k x}), since the
+// capped logit u = c log2e - 2 c log2e r falls as r grows (max u is that of min r).
+// Then t = u - m is one FMA per logit, and d, s follow.
 template <>
 struct Epilogue<EPI_FWD_STATS> {
   template <int CH>
@@ -236,6 +285,9 @@ struct Epilogue<EPI_FWD_STATS> {
     const float c = ea.softcap;
     const float k = cap ? 2.0f * kLog2e / c : 0.0f;
     const float c_l2 = c * kLog2e, m2c_l2 = -2.0f * c * kLog2e;
+    // u = A * v + B0 for the chunk value v (v = x without the cap, v = r with it)
+    const float A = cap ? m2c_l2 : kLog2e;
+    const float B0 = cap ? c_l2 : 0.0f;
     const int vcol0 = ea.col_base + col0;
     const bool smooth = ea.smooth != 0.0f;
     float mx = -1e30f, d = 0.0f, s = 0.0f, zy = 0.0f, sw = 0.0f;
@@ -248,7 +300,7 @@ struct Epilogue<EPI_FWD_STATS> {
       tmem_ld32(tbase + ch * 32, x);
       const int vb = vcol0 + ch * 32;
       const int nvalid = static_cast<int>(ea.V - vb);
-      if (zrow) {
+      if (zrow && FLCE_CHECK(row_run_ok(col0 + ch * 32, 32, ea.ld_z), ea.err)) {
         // 32-byte aligned: 256-aligned workspace, pitch a multiple of 256 floats
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_global_cs_v8f(zrow + ch * 32 + q * 8, x + q * 8);
@@ -260,58 +312,57 @@ struct Epilogue<EPI_FWD_STATS> {
           if (j == y - vb) zy = cap ? fmaf(-2.0f * c, softcap_r(x[j], k), c) : x[j];
         hit = true;
       }
-      // logits in log2 units (capped), and the smoothing sum of w_v z_v
+      float cm;  // the chunk's maximum of u
       if (cap) {
+        // x -> r = 1 / (1 + 2^{k x}), the lanes of softcap_r two at a time
         const uint64_t k2 = f2_pack(k, k), one2 = f2_pack(1.0f, 1.0f);
-        const uint64_t a2 = f2_pack(m2c_l2, m2c_l2), b2 = f2_pack(c_l2, c_l2);
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          // the lanes of softcap_r, two at a time
           float e0, e1, r0, r1;
           f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), k2), e0, e1);
           f2_unpack(f2_add(one2, f2_pack(fast_ex2(e0), fast_ex2(e1))), r0, r1);
-          r0 = fast_rcp(r0);
-          r1 = fast_rcp(r1);
-          if (smooth) {
-            if (j < nvalid)
-              sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, fmaf(-2.0f * c, r0, c), sw);
-            if (j + 1 < nvalid)
-              sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j + 1) : 1.0f, fmaf(-2.0f * c, r1, c), sw);
-          }
-          f2_unpack(f2_fma(a2, f2_pack(r0, r1), b2), x[j], x[j + 1]);
+          x[j] = fast_rcp(r0);
+          x[j + 1] = fast_rcp(r1);
         }
+        if (smooth) {  // sum of w_v z_v, natural units
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid)
+              sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, fmaf(-2.0f * c, x[j], c), sw);
+        }
+        if (nvalid < 32) {  // r lies in [0, 1]: 2 is never the minimum
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j >= nvalid) x[j] = 2.0f;
+        }
+        cm = fmaf(m2c_l2, min32(x), c_l2);
       } else {
         if (smooth) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < nvalid) sw = fmaf(ea.cw ? __ldg(ea.cw + vb + j) : 1.0f, x[j], sw);
         }
-        const uint64_t l2 = f2_pack(kLog2e, kLog2e);
+        if (nvalid < 32) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2)
-          f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), l2), x[j], x[j + 1]);
+          for (int j = 0; j < 32; ++j)
+            if (j >= nvalid) x[j] = -1e30f;
+        }
+        cm = kLog2e * max32(x);
       }
-      if (nvalid < 32) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j >= nvalid) x[j] = -1e30f;
-      }
-      float cm = x[0];
-#pragma unroll
-      for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
       if (cm > mx) {
         const float a = fast_ex2(mx - cm);
         s = a * fmaf(mx - cm, d, s);
         d *= a;
         mx = cm;
       }
+      const float B = B0 - mx;  // t = A v + B = u - m
       if (nvalid >= 32) {
         // two lanes of (d, s) per chunk, added into the running sums at its end
-        const uint64_t nmx = f2_pack(-mx, -mx);
+        const uint64_t A2 = f2_pack(A, A), B2 = f2_pack(B, B);
         uint64_t dd = f2_pack(0.0f, 0.0f), ss = dd;
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const uint64_t t = f2_add(f2_pack(x[j], x[j + 1]), nmx);
+          const uint64_t t = f2_fma(A2, f2_pack(x[j], x[j + 1]), B2);
           float t0, t1;
           f2_unpack(t, t0, t1);
           const uint64_t e = f2_pack(fast_ex2(t0), fast_ex2(t1));
@@ -326,14 +377,16 @@ struct Epilogue<EPI_FWD_STATS> {
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float t = x[j] - mx;
+          const float t = fmaf(A, x[j], B);
           const float e = (j < nvalid) ? fast_ex2(t) : 0.0f;
           d += e;
           s = fmaf(e, t, s);
         }
       }
     }
-    if (row_ok) {
+    if (row_ok && FLCE_CHECK(index_ok(vcol0 / (CH * 32), ea.n_parts) &&
+                                 index_ok(row, ea.part_stride),
+                             ea.err)) {
       const int64_t part = vcol0 / (CH * 32);
       const int64_t o = part * ea.part_stride + row;
       ea.pm[o] = mx;
@@ -441,7 +494,7 @@ struct Epilogue<EPI_DLOGITS> {
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && FLCE_CHECK(row_run_ok(col0 + ch * 32, 32, ea.ld_dl), ea.err)) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
@@ -469,7 +522,7 @@ struct Epilogue<EPI_STORE_BF16> {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int col = col0 + c * 32 + q * 8;
-        if (col < ea.cols) {
+        if (col < ea.cols && FLCE_CHECK(row_run_ok(ea.col_base + col, 8, ea.ld_out), ea.err)) {
           uint4 v = make_uint4(pack_bf16x2(x[q * 8 + 0], x[q * 8 + 1]),
                                pack_bf16x2(x[q * 8 + 2], x[q * 8 + 3]),
                                pack_bf16x2(x[q * 8 + 4], x[q * 8 + 5]),
@@ -497,7 +550,7 @@ struct Epilogue<EPI_ACCUM> {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int col = col0 + c * 32 + q * 8;
-        if (col >= ea.cols) continue;
+        if (col >= ea.cols || !FLCE_CHECK(row_run_ok(col, 8, ea.ld_acc), ea.err)) continue;
         // the fp32 accumulator lives in the workspace (256-aligned, pitch a multiple
         // of 8 floats): 32-byte aligned
         float* a = ea.acc + base + c * 32 + q * 8;
@@ -534,6 +587,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                           const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
                           const EpiArgs ea) {
   using C = PairCfg<TN, epi_warps<EPI>()>;
+  constexpr int EW = epi_warps<EPI>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -544,8 +598,11 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
   uint64_t* tempty = bars + 2 * C::STAGES + C::NACC;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 2 * C::NACC);
+  uint64_t* rfull = bars + 2 * C::STAGES + 2 * C::NACC;  // tile ring: slot written
+  uint64_t* rempty = rfull + TILE_RING;                  // tile ring: slot read by all
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(rempty + TILE_RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* ring = reinterpret_cast<volatile int*>(tmem_holder + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -562,7 +619,13 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * epi_warps<EPI>());
+      mbar_init(&tempty[a], 2 * EW);
+    }
+    for (int r = 0; r < TILE_RING; ++r) {
+      mbar_init(&rfull[r], 1);  // the scheduler publishes
+      // (peer's copy) read by: both producers, the leader's UMMA warp, every epilogue
+      // warp of both CTAs
+      mbar_init(&rempty[r], 3 + 2 * EW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -577,15 +640,34 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total = sh.m_tiles * sh.n_tiles;
+  constexpr uint32_t kSched = 1;  // the CTA whose warp 1 schedules the pair's tiles
+  const uint32_t rempty_sched = mapa_shared(smem_u32(&rempty[0]), kSched);
+
+  // The i-th tile of this pair, read from ring slot i % TILE_RING once published (a
+  // value >= total ends the schedule); the read is then acknowledged to the scheduler.
+  // The acknowledgement is a relaxed arrive: the acquire load orders it after the
+  // read, so the scheduler cannot overwrite the slot before it was read, and no role
+  // (the UMMA issuer in particular) waits for its own earlier memory operations.
+  auto take_tile = [&](int i, bool ack) -> int {
+    const int slot = i % TILE_RING;
+    if (!mbar_wait<true>(&rfull[slot], (i / TILE_RING) & 1, abort_flag, ea.err)) return total;
+    const int t = ld_acquire_shared(ring + slot);
+    if (ack) mbar_arrive_cluster_relaxed(rempty_sched + slot * 8);
+    return t;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs)
       const uint64_t pol_a = l2_policy(sh.a_hint);
       const uint64_t pol_b = l2_policy(sh.b_hint);
+      const uint32_t abort_peer =
+          mapa_shared(smem_u32(const_cast<int*>(abort_flag)), prank ^ 1u);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl) {
+      for (int i = 0; ok; ++i) {
+        const int t = take_tile(i, true);
+        if (t >= total) break;
         int mt, nt;
         tile_coords(t, sh, mt, nt);
         const int am0 = mt * PAIR_BM + static_cast<int>(prank) * 128 + sh.a_mn_off;
@@ -598,10 +680,21 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), kLead);
           if (prank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           const int k0 = kb * BK;
-          load_operand<A_MN, 128>(sA + stage * C::A_BYTES, &tmA, fb, am0, k0 + sh.a_k_off,
-                                  pol_a);
-          load_operand<B_MN, C::B_ROWS>(sB + stage * C::B_BYTES, &tmB, fb, bn0,
-                                        k0 + sh.b_k_off, pol_b);
+          const bool in_a = load_operand<A_MN, 128>(sA + stage * C::A_BYTES, &tmA, fb, am0,
+                                                    k0 + sh.a_k_off, pol_a, sh.a_inner,
+                                                    sh.a_outer);
+          const bool in_b = in_a && load_operand<B_MN, C::B_ROWS>(
+                                        sB + stage * C::B_BYTES, &tmB, fb, bn0,
+                                        k0 + sh.b_k_off, pol_b, sh.b_inner, sh.b_outer);
+          if (!in_b) {
+            // (FLCE_DEBUG build only) a box out of range was not loaded: its stage can
+            // never fill, so stop both CTAs of the pair instead of letting them wait
+            atomicOr(ea.err, FLCE_DEVERR_BOUNDS);
+            *abort_flag = 1;
+            st_shared_cluster_u32(abort_peer, 1u);
+            ok = false;
+            break;
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -619,14 +712,41 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
       }
     }
     __syncwarp();
+  } else if (warp == 1 && prank == kSched) {
+    if (lane == 0) {
+      // ---------------- tile scheduler (the peer CTA's warp 1)
+      const uint32_t ring_lead = mapa_shared(smem_u32(const_cast<int*>(ring)), kLead);
+      const uint32_t rfull_lead = mapa_shared(smem_u32(&rfull[0]), kLead);
+      int t = cid;  // the pair's first tile; later ones come from the counter
+      for (int i = 0;; ++i) {
+        const int slot = i % TILE_RING;
+        if (!mbar_wait<true>(&rempty[slot], ((i / TILE_RING) & 1) ^ 1u, abort_flag, ea.err))
+          break;
+        ring[slot] = t;
+        st_shared_cluster_u32(ring_lead + slot * 4, static_cast<uint32_t>(t));
+        mbar_arrive_local(&rfull[slot]);
+        mbar_arrive_cluster(rfull_lead + slot * 8);
+        if (t >= total) break;
+        t = ncl + static_cast<int>(atomicAdd(sh.sched, 1u));
+      }
+      // this pair draws no more tiles; the last pair to get here resets the counters
+      // (every other pair's draws happened before its increment)
+      __threadfence();
+      if (atomicAdd(sh.sched + 1, 1u) == static_cast<unsigned int>(ncl - 1)) {
+        __threadfence();
+        atomicExch(sh.sched, 0u);
+        atomicExch(sh.sched + 1, 0u);
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && prank == 0) {
       // ---------------- UMMA issuer (pair leaders only)
       constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, TN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0;
-      int it = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl, ++it) {
+      for (int it = 0; ok; ++it) {
+        if (take_tile(it, true) >= total) break;
         const int acc = it % C::NACC;
         const uint32_t aph = (it / C::NACC) & 1;
         // the epilogues of both CTAs arrive here (cluster-scope acquire)
@@ -664,8 +784,11 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), kLead);
-    int it = 0;
-    for (int t = cid; t < total; t += ncl, ++it) {
+    for (int it = 0;; ++it) {
+      const int t = take_tile(it, false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(rempty_sched + (it % TILE_RING) * 8);
+      if (t >= total) break;
       int mt, nt;
       tile_coords(t, sh, mt, nt);
       const int acc = it % C::NACC;
@@ -674,9 +797,11 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TN +
                              half * C::EPI_COLS;
-      Epilogue<EPI>::template run<C::EPI_CHUNKS>(
-          ea, tbase, mt * PAIR_BM + static_cast<int>(prank) * 128 + r,
-          nt * TN + half * C::EPI_COLS);
+      if (FLCE_CHECK(tmem_ok(acc * TN + half * C::EPI_COLS, C::EPI_CHUNKS * 32, q, warp),
+                     ea.err))
+        Epilogue<EPI>::template run<C::EPI_CHUNKS>(
+            ea, tbase, mt * PAIR_BM + static_cast<int>(prank) * 128 + r,
+            nt * TN + half * C::EPI_COLS);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -702,6 +827,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (sh.m_tiles <= 0 || sh.n_tiles <= 0) return cudaSuccess;
+  if (!sh.sched) return cudaErrorInvalidValue;  // the dynamic schedule's counters
   constexpr int csize = 2;
   const int total = sh.m_tiles * sh.n_tiles;
   cudaLaunchAttribute attr[1];

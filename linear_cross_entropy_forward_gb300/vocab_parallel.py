@@ -7,7 +7,9 @@ PR #551 review calls m and d of the first online-softmax pass, plus the centred 
 the entropy needs -- the ranks all-gather them, and each merges the [P, 4, N] block by
 max-rescaling into lse, E_p[z], CE and entropy for the whole vocabulary.  The backward
 needs one more: each rank's dhidden is its slice's term, summed by an all-reduce;
-dweight stays sharded.  Labels, hidden and the upstream gradients are replicated.
+dweight stays sharded.  The terms are kept in fp32 (the backward's unrounded
+accumulation) for the sum, which is rounded to hidden's dtype once, after it.
+Labels, hidden and the upstream gradients are replicated.
 """
 from __future__ import annotations
 
@@ -31,7 +33,8 @@ def exchange_stats(local_stats: torch.Tensor, group=None) -> torch.Tensor:
 
 
 def reduce_dhidden(dh_partial: torch.Tensor, group=None) -> torch.Tensor:
-    """Sum each rank's dhidden term over the ranks (in fp32, fp64 stays fp64)."""
+    """Sum each rank's dhidden term over the ranks (in fp32, fp64 stays fp64); the
+    result has the term's dtype."""
     import torch.distributed as dist
     acc = dh_partial.double() if dh_partial.dtype == torch.float64 else dh_partial.float()
     if dist.is_available() and dist.is_initialized():
@@ -68,9 +71,9 @@ class _VocabParallelCE(torch.autograd.Function):
         dh, dw = B.flce_backward(hidden, weight_shard, labels, lse, ez, prep(g_loss), prep(g_ent),
                                  reduction, ignore_index, zloss_coef, softcap,
                                  weight_layout=weight_layout, v_offset=v_offset,
-                                 v_total=v_total)
-        return (reduce_dhidden(dh, group), dw, None, None, None, None, None, None, None, None,
-                None)
+                                 v_total=v_total, dhidden_fp32=True)
+        return (reduce_dhidden(dh, group).to(hidden.dtype), dw, None, None, None, None, None,
+                None, None, None, None)
 
 
 def vocab_parallel_linear_cross_entropy(hidden, weight_shard, labels, v_offset, v_total,

@@ -46,14 +46,14 @@ def test_error_codes_match_the_header():
     """Every FLCE_ERR_* code of the header has its name in the binding's error messages."""
     codes = dict((name, int(v)) for name, v in
                  re.findall(r"FLCE_ERR_([A-Z_]+)\s*=\s*(\d+)", open(HEADER).read()))
-    assert codes and max(codes.values()) == 9
+    assert codes and max(codes.values()) == 10
     assert {v: k for k, v in codes.items()} == B._ERR_NAMES
 
 
 def test_params_struct_layout():
-    # int64 x4, int32, float, float, int32, int64, int32, float, pointer, int64 x3
-    # -> 96 bytes, as in flce.h
-    assert ctypes.sizeof(B.FlceParams) == 96
+    # int64 x4, int32, float, float, int32, int64, int32, float, pointer, int64 x3, int32
+    # (+ 4 bytes of tail padding) -> 104 bytes, as in flce.h
+    assert ctypes.sizeof(B.FlceParams) == 104
     assert B.FlceParams.chunk_v.offset == 48
     assert B.FlceParams.weight_layout.offset == 56
     assert B.FlceParams.label_smoothing.offset == 60
@@ -61,6 +61,7 @@ def test_params_struct_layout():
     assert B.FlceParams.v_offset.offset == 72
     assert B.FlceParams.v_total.offset == 80
     assert B.FlceParams.chunk_n.offset == 88
+    assert B.FlceParams.dhidden_fp32.offset == 96
 
 
 def test_params_struct_matches_the_c_compiler(tmp_path):
@@ -69,17 +70,18 @@ def test_params_struct_matches_the_c_compiler(tmp_path):
     src = tmp_path / "t.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "flce.h"\n'
-        'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(flce_params),'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(flce_params),'
         ' offsetof(flce_params, chunk_v), offsetof(flce_params, class_weight),'
         ' offsetof(flce_params, v_offset), offsetof(flce_params, v_total),'
-        ' offsetof(flce_params, chunk_n)); return 0;}\n')
+        ' offsetof(flce_params, chunk_n), offsetof(flce_params, dhidden_fp32)); return 0;}\n')
     exe = tmp_path / "t"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
                    check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     F = B.FlceParams
     assert [int(x) for x in out] == [ctypes.sizeof(F), F.chunk_v.offset, F.class_weight.offset,
-                                     F.v_offset.offset, F.v_total.offset, F.chunk_n.offset]
+                                     F.v_offset.offset, F.v_total.offset, F.chunk_n.offset,
+                                     F.dhidden_fp32.offset]
 
 
 def test_workspace_sizes(lib):
@@ -96,6 +98,10 @@ def test_workspace_sizes(lib):
     assert flce.kernel_launches(p2, 1) == 1 + 3 * 4
     assert flce.kernel_launches(p2, 0) == 2
     assert flce.kernel_launches(flce.make_params(300, 200, 1000, "sum"), 0) == 3
+    # an fp32 dhidden is its own accumulator: no fp32 workspace copy of it
+    p3 = flce.make_params(300, 200, 1000, "none", chunk_v=256, dhidden_fp32=True)
+    assert flce.workspace_size(p3, 1) == flce.workspace_size(p2, 1) - ((300 * 200 * 4 + 255)
+                                                                       // 256 * 256)
 
 
 def test_fused_workspace_and_launches(lib):
@@ -168,6 +174,51 @@ def test_fused_rejects_shards_nulls_alignment_and_small_workspace(lib):
     mis[10] = bad  # dweight
     assert lib.flce_forward_backward(ctypes.byref(p), *mis, 1 << 20, None) == 3
     assert lib.flce_forward_backward(ctypes.byref(p), *args, 16, None) == 4
+
+
+def test_vocabulary_alignment_applies_to_the_hv_layout_only(lib):
+    """V is a row length only in the [H,V] layout; a [V,H] weight takes any V."""
+    for V in (1, 7, 1001, 50257):
+        p = flce.make_params(10, 64, V, "mean", weight_layout="vh")
+        for phase in (0, 1, 3):
+            assert lib.flce_workspace_size(ctypes.byref(p), phase) > 0
+        q = flce.make_params(10, 64, V, "mean", weight_layout="hv")
+        assert lib.flce_workspace_size(ctypes.byref(q), 0) == 0
+        fake = ctypes.c_void_p(0x1000)
+        assert lib.flce_forward(ctypes.byref(q), fake, fake, fake, fake, fake, fake, fake, fake,
+                                1 << 20, None) == 3
+    # H is a row length in both layouts
+    p = flce.make_params(10, 60, 64, "mean", weight_layout="vh")
+    assert lib.flce_workspace_size(ctypes.byref(p), 0) == 0
+
+
+def test_check_params_gives_the_entry_points_status(lib):
+    """flce_check_params returns the status the entry points return for the same
+    parameters, and the binding raises it (not a generic BAD_ARG) when sizing."""
+    cases = [(dict(N=10, H=64, V=100), 3), (dict(N=10, H=4, V=64), 2),
+             (dict(N=10, H=64, V=64, chunk_v=100), 1), (dict(N=10, H=64, V=100,
+                                                             weight_layout="vh"), 0)]
+    for kw, code in cases:
+        p = flce.make_params(kw.pop("N"), kw.pop("H"), kw.pop("V"), "mean", **kw)
+        assert lib.flce_check_params(ctypes.byref(p)) == code
+        if code:
+            with pytest.raises(B.FlceError) as ei:
+                flce.workspace_size(p, 0)
+            assert ei.value.code == code
+    assert lib.flce_check_params(None) == 1
+
+
+def test_fp32_dhidden_needs_32_byte_alignment_and_a_flag_of_0_or_1(lib):
+    ok = ctypes.c_void_p(0x10000)
+    half = ctypes.c_void_p(0x10010)  # 16-byte aligned, not 32
+    p = flce.make_params(10, 64, 64, "mean", dhidden_fp32=True)
+    args = [ok] * 7 + [half, ok, ok]  # dhidden is the 8th pointer
+    assert lib.flce_backward(ctypes.byref(p), *args, 1 << 20, None) == 3
+    p16 = flce.make_params(10, 64, 64, "mean")  # a bf16 dhidden may sit there
+    assert lib.flce_backward(ctypes.byref(p16), *args, 16, None) == 4  # gets past alignment
+    p.dhidden_fp32 = 2
+    assert lib.flce_workspace_size(ctypes.byref(p), 1) == 0
+    assert lib.flce_backward(ctypes.byref(p), *([ok] * 10), 1 << 20, None) == 1
 
 
 def test_scale_bf16_argument_checks(lib):

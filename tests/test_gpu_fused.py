@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import _fullsize_oracle as fso
 from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward,
                                                 flce_forward_backward, flce_scale_bf16,
                                                 linear_cross_entropy)
@@ -83,7 +84,13 @@ CASES = [
                                            ignore_frac=0.15), 0),
     ("one_row", dataclasses.replace(W0, name="f7", N=1, H=8, V=8, ignore_frac=0.0), 0),
 ]
-LAYOUT_CASES = [c for c in CASES if c[0] in ("ragged_none_chunks", "softcap_30", "tiny")]
+LAYOUT_CASES = [c for c in CASES if c[0] in ("ragged_none_chunks", "softcap_30", "tiny")] + [
+    # a [V,H] weight takes any vocabulary size (not a multiple of 8 here)
+    ("odd_vocab_chunks", dataclasses.replace(W0, name="f8", N=1100, H=200, V=1001,
+                                             reduction="none", grad_mode="normal"), 512),
+    ("odd_vocab_mean_cap", dataclasses.replace(W0, name="f9", N=300, H=128, V=2003, w_std=0.2,
+                                               softcap=4.0, zloss_coef=1e-3), 0),
+]
 
 
 def check_against_oracle(w, chunk_n, layout="hv", eps=0.0, cw=None):
@@ -250,7 +257,8 @@ FULL = [wl.LLAMA3, wl.QWEN25]
 def test_fused_fullsize_against_two_call_and_oracle_rows(w):
     """Bench-size workloads with the default token chunk (Llama-3 head: one chunk;
     Qwen2.5 RL batch: two, with fp32 dweight accumulation): forward outputs bitwise
-    equal to the two-call path, gradients close to it, dhidden rows against the oracle."""
+    equal to the two-call path, gradients close to it; every row's lse and E_p[z],
+    sampled dhidden rows and sampled dweight columns against the oracle."""
     _cuda_or_skip()
     dev = torch.device("cuda")
     label_dev = "cuda" if w.label_mode == "self" else "cpu"
@@ -270,17 +278,23 @@ def test_fused_fullsize_against_two_call_and_oracle_rows(w):
     assert float((dh.float() - dh2.float()).norm() / dh2.float().norm()) <= 4e-3
     assert float((dw.float() - dw2.float()).norm() / dw2.float().norm()) <= 4e-3
     del dh2, dw2
+    # every row's forward outputs against the oracle (row statistics cached per process)
+    hb, wb = wl.bf16_bits(hidden), wl.bf16_bits(weight)
+    h64 = orc.bf16_bits_to_f64(hb)
+    W64 = orc.bf16_bits_to_f64(wb)
+    y = labels.cpu().numpy()
+    st = fso.row_stats(hb, wb, h64, W64, w.softcap)
+    o = orc.forward(h64, W64, y, "none", stats=st, **kw)
+    assert np.abs(f64(lse) - o["lse"]).max() <= TOK_ABS
+    assert np.abs(f64(ez) - o["ez"]).max() <= TOK_ABS
+    # dhidden on sampled rows, dweight on sampled columns (with several token chunks the
+    # columns hold the fp32 accumulation across chunks)
     rng = np.random.default_rng(99)
     rows = np.unique(np.concatenate([rng.choice(w.N, 24, replace=False), [0, w.N - 1]]))
-    h64 = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
-    W64 = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
-    y = labels.cpu().numpy()
-    o = orc.forward(h64[rows], W64, y[rows], "none", **kw)
-    assert np.abs(f64(lse)[rows] - o["lse"]).max() <= TOK_ABS
-    lse_full = np.zeros(w.N)
-    ez_full = np.zeros(w.N)
-    lse_full[rows] = o["lse"]
-    ez_full[rows] = o["ez"]
-    dh_o, _ = orc.backward(h64, W64, y, lse_full, ez_full, g_loss.numpy(), g_ent.numpy(),
+    dh_o, _ = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.numpy(), g_ent.numpy(),
                            w.reduction, rows=rows, **kw)
     assert rel_l2(f64(dh[torch.from_numpy(rows).to(dev)]), dh_o) <= GRAD_REL_L2
+    cols = fso.dweight_columns(w.V, y)
+    _, dw_o = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.numpy(), g_ent.numpy(),
+                           w.reduction, cols=cols, **kw)
+    assert rel_l2(f64(dw[:, torch.from_numpy(cols).to(dev)]), dw_o) <= GRAD_REL_L2

@@ -155,6 +155,47 @@ def test_parity_weight_vh(name, w, chunk_v):
     print(name, "vh", rep)
 
 
+# A [V,H] weight takes any vocabulary size: V is not a row length there, so it needs no
+# multiple of 8 (the [H,V] layout does).  GPT-2's 50257 among them.
+VH_ODD_VOCAB_CASES = [
+    ("odd_none_chunks", dataclasses.replace(W0, name="o1", N=300, H=200, V=1001,
+                                            reduction="none", grad_mode="normal"), 256),
+    ("gpt2_vocab_mean_zloss", dataclasses.replace(W0, name="o2", N=256, H=256, V=50257,
+                                                  zloss_coef=1e-4), 0),
+    ("odd_softcap_sum", dataclasses.replace(W0, name="o3", N=130, H=64, V=777, w_std=0.3,
+                                            softcap=3.0, reduction="sum"), 256),
+    ("one_class_column_past_tile", dataclasses.replace(W0, name="o4", N=64, H=16, V=257,
+                                                       ignore_frac=0.0), 0),
+]
+
+
+@pytest.mark.parametrize("name,w,chunk_v", VH_ODD_VOCAB_CASES,
+                         ids=[c[0] for c in VH_ODD_VOCAB_CASES])
+def test_parity_weight_vh_any_vocabulary_size(name, w, chunk_v):
+    _cuda_or_skip()
+    rep = {}
+    check_parity(w, chunk_v, rep, weight_layout="vh")
+    print(name, "vh", rep)
+
+
+def test_parity_weight_vh_odd_vocabulary_smoothing_and_class_weights():
+    _cuda_or_skip()
+    w = dataclasses.replace(W0, name="o5", N=300, H=200, V=999, reduction="mean")
+    cw = torch.rand(w.V, generator=torch.Generator().manual_seed(5)) * 1.5 + 0.25
+    check_parity(w, 256, {}, weight_layout="vh", eps=0.1, cw=cw)
+
+
+def test_hv_weight_refuses_a_vocabulary_that_is_not_a_multiple_of_8():
+    _cuda_or_skip()
+    from linear_cross_entropy_forward_gb300 import FlceError
+    dev = torch.device("cuda")
+    h = torch.zeros(4, 16, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(4, dtype=torch.int64, device=dev)
+    with pytest.raises(FlceError) as ei:
+        flce_forward(h, torch.zeros(16, 1001, dtype=torch.bfloat16, device=dev), y, "mean")
+    assert ei.value.code == 3
+
+
 SMOOTH_CASES = [
     # (name, workload, chunk_v, label_smoothing, class weights?)
     ("smooth_mean", dataclasses.replace(W0, name="ls1", N=300, H=200, V=1000), 256, 0.1, False),

@@ -1,7 +1,9 @@
 """Vocabulary-parallel path on one GPU: the shards run one after another through
 flce_shard_stats -> flce_combine_shards -> flce_backward (per shard) and must match the
-whole-vocabulary fp64 oracle (tolerances as in the other parity tests); the
-single-rank autograd wrapper must match the unsharded entry points."""
+whole-vocabulary fp64 oracle (tolerances as in the other parity tests); the shards'
+dhidden terms come back in fp32 (dhidden_fp32) and are summed before one rounding, as
+the all-reduce of the multi-GPU path sums them; the single-rank autograd wrapper must
+match the unsharded entry points."""
 import dataclasses
 
 import numpy as np
@@ -42,6 +44,14 @@ CASES = [
     ("sum_vh_4shards", dataclasses.replace(wl.TINY, name="vp3", N=260, H=128, V=776,
                                            reduction="sum"),
      [0, 200, 392, 584, 776], "vh"),
+    # eight uneven shards, ragged in every dimension
+    ("mean_8shards", dataclasses.replace(wl.TINY, name="vp5", N=520, H=192, V=4104,
+                                         zloss_coef=1e-3),
+     [0, 8, 520, 1032, 1800, 2056, 3080, 3600, 4104], "hv"),
+    ("none_vh_8shards_cap", dataclasses.replace(wl.TINY, name="vp6", N=300, H=128, V=2048,
+                                                reduction="none", grad_mode="normal",
+                                                w_std=0.2, softcap=5.0),
+     [0, 256, 512, 768, 1024, 1280, 1536, 1792, 2048], "vh"),
 ]
 
 
@@ -65,9 +75,12 @@ def test_sequential_shards_match_oracle(name, w, cuts, layout):
     for a, ws in shards:
         dhp, dwp = flce_backward(hd, ws, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
                                  zloss_coef=w.zloss_coef, softcap=w.softcap, validate=True,
-                                 weight_layout=layout, v_offset=a, v_total=w.V)
-        dh += dhp.float()
+                                 weight_layout=layout, v_offset=a, v_total=w.V,
+                                 dhidden_fp32=True)
+        assert dhp.dtype == torch.float32
+        dh += dhp
         dws.append(dwp if layout == "hv" else dwp.t())
+    dh = dh.to(torch.bfloat16)  # one rounding of the sum, as after the all-reduce
     dw = torch.cat(dws, dim=1)
     torch.cuda.synchronize()
 
@@ -111,3 +124,26 @@ def test_single_rank_wrapper_matches_unsharded_path():
                            "mean", zloss_coef=1e-3)
     assert rel_l2(h.grad.float().cpu().numpy(), dh.float().cpu().numpy()) <= 1e-3
     assert rel_l2(W.grad.float().cpu().numpy(), dw.float().cpu().numpy()) <= 1e-3
+
+
+@pytest.mark.parametrize("chunk_v", [0, 256])
+def test_fp32_dhidden_rounds_to_the_bf16_dhidden(chunk_v):
+    """dhidden_fp32 returns the fp32 accumulation the bf16 output is rounded from: one
+    vocabulary chunk (the tile's accumulator) or several (the fp32 sum over chunks), the
+    same sums in the same order, so rounding it gives the bf16 output's bits."""
+    _cuda_or_skip()
+    dev = torch.device("cuda")
+    w = dataclasses.replace(wl.TINY, name="vp7", N=300, H=136, V=1000, zloss_coef=1e-3,
+                            softcap=8.0)
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    _, _, lse, ez = flce_forward(hd, Wd, yd, w.reduction, zloss_coef=1e-3, softcap=8.0)
+    kw = dict(zloss_coef=1e-3, softcap=8.0, chunk_v=chunk_v, validate=True)
+    dh16, dw16 = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
+                               **kw)
+    dh32, dw32 = flce_backward(hd, Wd, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
+                               dhidden_fp32=True, **kw)
+    torch.cuda.synchronize()
+    assert dh32.dtype == torch.float32
+    assert torch.equal(dh32.to(torch.bfloat16).view(torch.int16), dh16.view(torch.int16))
+    assert torch.equal(dw32.view(torch.int16), dw16.view(torch.int16))

@@ -1,4 +1,4 @@
-"""The vocabulary-parallel exchange on two CPU ranks (gloo).
+"""The vocabulary-parallel exchange on CPU ranks (gloo): two, three and eight.
 
 Each rank holds half of the vocabulary, computes its shard's softmax statistics with
 the oracle, exchanges them with the package's exchange_stats (an all-gather), merges
@@ -69,6 +69,12 @@ def test_two_rank_vocab_parallel_exchange(reduction, cap):
 
 def test_three_rank_vocab_parallel_exchange():
     mp.spawn(_worker, args=(3, _free_port(), "mean", 1.5), nprocs=3, join=True)
+
+
+def test_eight_rank_vocab_parallel_exchange():
+    """Eight shards of 10-11 columns each: the all-gather of the statistics, the merge and
+    the all-reduce of the dhidden terms against the whole-vocabulary oracle."""
+    mp.spawn(_worker, args=(8, _free_port(), "none", 2.0), nprocs=8, join=True)
 
 
 def _worker_peer_leaves(rank, world, port, flag_path):
