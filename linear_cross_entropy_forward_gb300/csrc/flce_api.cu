@@ -891,9 +891,8 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
         p->class_weight, rowc, rowd);
     if ((rc = cuda_rc(cudaGetLastError()))) return rc;
     {
-      const int64_t row_steps = cdiv(rows, kDlzRows);
       const dim3 grid(static_cast<unsigned>(cdiv(L.ldz, kDlzCols)),
-                      static_cast<unsigned>(row_steps < 65535 ? row_steps : 65535));
+                      static_cast<unsigned>(rows < 65535 ? rows : 65535));
       dlogits_from_z_kernel<<<grid, kDlzThreads, 0, st>>>(
           so.zout, rows, L.ldz, rowc, rowd, lab, V, p->softcap, smooth ? 1 : 0,
           p->class_weight, dl);

@@ -32,10 +32,9 @@ struct Parts {
   int64_t part_stride;
 };
 
-// dlogits_from_z_kernel: threads per block, columns per block, rows per block step
+// dlogits_from_z_kernel: threads per block, columns per block
 constexpr int kDlzThreads = 256;
 constexpr int kDlzCols = 2 * 8 * kDlzThreads;  // columns per block
-constexpr int kDlzRows = 2;
 
 __global__ void __launch_bounds__(256) fwd_combine_kernel(
     Parts pt, int64_t N, const float* __restrict__ zlabel, const int64_t* __restrict__ labels,
