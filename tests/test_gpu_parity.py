@@ -328,3 +328,37 @@ def test_binding_rejects_mismatched_outputs_and_workspace():
                               out=(torch.empty(64, **f32),) * 4 + (dh, dh))
     with pytest.raises(TypeError):  # a CPU tensor among CUDA ones
         flce_forward(hidden, weight, labels.cpu(), "none")
+
+
+def test_schedule_counters_are_zero_after_every_call():
+    """The GEMMs draw their tiles from two counters in the workspace header (bytes
+    128-135); the last CTA pair of each GEMM resets them, so after a call that ran many
+    GEMMs on one workspace (a backward of four vocabulary chunks: 12 GEMMs; a gradient-
+    in-forward call of three token chunks: 9) they are zero again, and results are right."""
+    _cuda_or_skip()
+    from linear_cross_entropy_forward_gb300 import (flce_forward_backward, make_params,
+                                                    workspace_size)
+    dev = torch.device("cuda")
+    w = dataclasses.replace(W0, name="sc", N=1100, H=200, V=1000, reduction="none",
+                            grad_mode="normal")
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    gl, ge = g_loss.to(dev), g_ent.to(dev)
+    p1 = make_params(w.N, w.H, w.V, "none", chunk_v=256)
+    ws_f = torch.full((workspace_size(p1, 0),), 7, dtype=torch.uint8, device=dev)
+    ws_b = torch.full((workspace_size(p1, 1),), 7, dtype=torch.uint8, device=dev)
+    p3 = make_params(w.N, w.H, w.V, "none", chunk_n=512)
+    ws_g = torch.full((workspace_size(p3, 3),), 7, dtype=torch.uint8, device=dev)
+    for _ in range(2):  # the second round starts from the counters the first left
+        _, _, lse, ez = flce_forward(hd, Wd, yd, "none", validate=True, workspace=ws_f)
+        dh, dw = flce_backward(hd, Wd, yd, lse, ez, gl, ge, "none", validate=True, chunk_v=256,
+                               workspace=ws_b)
+        out = flce_forward_backward(hd, Wd, yd, gl, ge, "none", validate=True, chunk_n=512,
+                                    workspace=ws_g)
+        torch.cuda.synchronize()
+        for ws in (ws_f, ws_b, ws_g):
+            assert torch.all(ws[128:136] == 0), ws[128:136].tolist()
+    o, dh_o, dw_o = oracle_run(w, hidden, weight, labels, g_loss, g_ent)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    assert rel_l2(f(dh), dh_o) <= GRAD_REL_L2 and rel_l2(f(dw), dw_o) <= GRAD_REL_L2
+    assert rel_l2(f(out[4]), dh_o) <= GRAD_REL_L2 and rel_l2(f(out[5]), dw_o) <= GRAD_REL_L2
