@@ -32,7 +32,7 @@ namespace flce {
 
 namespace {
 
-constexpr int kVersion = 200;  // 0.2.0
+constexpr int kVersion = 300;  // 0.3.0: flce_params.dhidden_fp32, flce_check_params, FLCE_ERR_BOUNDS, flce_plan_tiles without operand sharing
 constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 // dlogits chunk target of the backward: fewer, wider chunks mean fewer fp32 passes

@@ -35,7 +35,7 @@ def test_header_declares_the_exported_set(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.flce_version() == 200
+    assert lib.flce_version() == 300
     for code in range(0, 10):
         assert lib.flce_strerror(code)
         assert b"unknown" not in lib.flce_strerror(code)
