@@ -40,7 +40,11 @@
  *     labels: int64.  Everything else: fp32.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *     enqueued asynchronously on it; nothing synchronises unless params->validate
- *     is set.
+ *     is set.  The backward passes run their dweight GEMM beside dhidden on an
+ *     internal stream (one per host thread and device, created on first use) that
+ *     is forked from `stream` by an event and joined back before the call returns,
+ *     so every call's work still follows the work enqueued on `stream` before it and
+ *     precedes the work enqueued after it.
  *   - Return value: FLCE_OK or one of the FLCE_ERR_* codes below.  Argument errors
  *     are detected on the host before anything is enqueued.  Device-side
  *     conditions (a label outside [0,V) that is not ignore_index, a pipeline wait
@@ -102,7 +106,7 @@ typedef struct {
   float softcap;         /* tanh logit soft-cap c, 0 = off */
   int32_t validate;      /* != 0: synchronise at the end and report device errors */
   int64_t chunk_v;       /* backward vocabulary chunk width (multiple of 256), 0 = auto:
-                          * the widest whose bf16 dlogits [N, chunk_v] fit 1 GiB */
+                          * the widest whose bf16 dlogits [N, chunk_v] fit 2 GiB */
   int32_t weight_layout; /* flce_weight_layout: how weight and dweight are stored */
   float label_smoothing; /* eps in [0, 1], 0 = off */
   const float* class_weight; /* [V] fp32 device pointer, per-class target weights; NULL = all 1 */

@@ -36,9 +36,11 @@ constexpr int kVersion = 300;  // 0.3.0: flce_params.dhidden_fp32, flce_check_pa
 constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 // dlogits chunk target of the backward: fewer, wider chunks mean fewer fp32 passes
-// over the dhidden accumulator and longer k-loops (1 GB measured 3-4 % faster than
-// 256 MB on the Llama-3, Qwen2.5 and Gemma-2 head shapes)
-constexpr int64_t kDefaultChunkBytes = int64_t(1) << 30;
+// over the dhidden accumulator, fewer partly idle last rounds of tiles and longer
+// k-loops (1 GiB measured 3-4 % faster than 256 MB on the Llama-3, Qwen2.5 and Gemma-2
+// head shapes; 2 GiB 0.3-0.5 % faster than 1 GiB on Llama-3 and Qwen2.5, the same on
+// Gemma-2; 4 GiB no faster than 2)
+constexpr int64_t kDefaultChunkBytes = int64_t(2) << 30;
 
 // Descriptor strides of the MN-major operand tiles: 64-wide MN atoms 8 KB apart
 // (leading byte offset), 8-row K groups 1 KB apart (stride byte offset).
@@ -55,12 +57,15 @@ struct FwdLayout {
 };
 
 constexpr size_t kWsumOffset = 64;  // float in the workspace header: sum of class weights
-// two uint32 counters of the GEMMs' dynamic tile schedule in the workspace header
-// (zeroed with the header at the start of every call, and by each GEMM at its end)
+// Pairs of uint32 counters of the GEMMs' dynamic tile schedule in the workspace header
+// (zeroed with the header at the start of every call, and by each GEMM at its end):
+// slot 0 for the GEMMs on the caller's stream, slot 1 for dweight, which runs beside
+// dhidden on the side stream.
 constexpr size_t kSchedOffset = 128;
 
-inline unsigned int* sched_counters(uint32_t* header) {
-  return reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(header) + kSchedOffset);
+inline unsigned int* sched_counters(uint32_t* header, int slot = 0) {
+  return reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(header) + kSchedOffset +
+                                         8 * slot);
 }
 
 FwdLayout fwd_layout(const flce_params* p) {
@@ -293,6 +298,51 @@ int read_status(const void* workspace, cudaStream_t st) {
 }
 
 inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
+
+// dweight and dhidden read the same dlogits and write different outputs, so they run
+// concurrently: dhidden on the caller's stream, dweight on a side stream forked from it
+// after the dlogits and joined back before anything reads or rewrites them.  dhidden is
+// launched first and takes every SM; as its pairs run out of tiles (its last round of
+// tiles is only partly full), dweight's pairs start on the SMs they free, and the
+// dynamic tile schedule balances the work between them.  The side stream and its two
+// events are created once per host thread and device: events are never shared between
+// threads, and a stream wait binds to the record before it, so reusing them across one
+// thread's calls is safe.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+int side_stream(SideStream** out) {
+  thread_local SideStream cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FLCE_ERR_CUDA;
+  SideStream& ss = cache[dev];
+  if (!ss.stream) {
+    SideStream n;
+    if (cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
+      if (n.fork) cudaEventDestroy(n.fork);
+      cudaStreamDestroy(n.stream);
+      return FLCE_ERR_CUDA;
+    }
+    ss = n;
+  }
+  *out = &ss;
+  return FLCE_OK;
+}
+
+// Fork: `side` waits for the work enqueued on `st` so far.  Join: `st` waits for `side`.
+int fork_side(const SideStream& ss, cudaStream_t st) {
+  int rc = cuda_rc(cudaEventRecord(ss.fork, st));
+  return rc ? rc : cuda_rc(cudaStreamWaitEvent(ss.stream, ss.fork, 0));
+}
+int join_side(const SideStream& ss, cudaStream_t st) {
+  int rc = cuda_rc(cudaEventRecord(ss.join, ss.stream));
+  return rc ? rc : cuda_rc(cudaStreamWaitEvent(st, ss.join, 0));
+}
 
 // a_hint / b_hint: the operand whose panels every tile of a group revisits keeps
 // its L2 lines (evict_last).  The streamed operand keeps the normal policy: with
@@ -674,6 +724,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     return p->validate ? read_status(ws, st) : FLCE_OK;
   }
 
+  SideStream* ss = nullptr;
+  if ((rc = side_stream(&ss))) return rc;
   float4* rowc = reinterpret_cast<float4*>(ws + L.rowc);
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(ws + L.dl);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
@@ -741,7 +793,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     // (rows v, hidden revisited as B).  Both operands are MN-major views.
     GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.k_blocks = static_cast<int>(cdiv(N, BK));
-    s4.sched = sched_counters(err);
+    s4.sched = sched_counters(err, 1);
     EpiArgs e4{};
     e4.V = V;
     e4.err = err;
@@ -767,9 +819,6 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
       e4.ld_out = V;
     }
     set_extents(&s4, vh ? mDlMn : mHidMn, vh ? mHidMn : mDlMn);
-    if ((rc = cuda_rc(vh ? launch_bwd_dweight(mDlMn.m, mHidMn.m, s4, e4, st)
-                         : launch_bwd_dweight(mHidMn.m, mDlMn.m, s4, e4, st))))
-      return rc;
 
     // dhidden (+)= dlogits @ weight[:, v0:v0+w]^T
     // the weight chunk is revisited by every row tile; dlogits rows streamed
@@ -801,9 +850,16 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
     }
     e5.err = err;
     set_extents(&s5, mDlK, mWDh);
+
+    // dhidden on the caller's stream, dweight beside it on the side stream (SideStream)
+    if ((rc = fork_side(*ss, st))) return rc;
     if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK.m, mWDh.m, s5, e5,
                                                                         st))))
       return rc;
+    if ((rc = cuda_rc(vh ? launch_bwd_dweight(mDlMn.m, mHidMn.m, s4, e4, ss->stream)
+                         : launch_bwd_dweight(mHidMn.m, mDlMn.m, s4, e4, ss->stream))))
+      return rc;
+    if ((rc = join_side(*ss, st))) return rc;
   }
   return p->validate ? read_status(ws, st) : FLCE_OK;
 }
@@ -840,6 +896,8 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
   const bool vh = p->weight_layout == FLCE_WEIGHT_VH;
   const bool per_token = p->reduction == FLCE_RED_NONE;
   const bool smooth = p->label_smoothing != 0.0f;
+  SideStream* ss = nullptr;
+  if ((rc = side_stream(&ss))) return rc;
   Smoothing sm{p->label_smoothing, p->class_weight, reinterpret_cast<float*>(ws + L.psw),
                nullptr};
   if (smooth && p->class_weight) {
@@ -929,6 +987,8 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     }
     e5.err = err;
     set_extents(&s5, mDlK, mWDh);
+    // dhidden on the caller's stream, dweight beside it on the side stream (SideStream)
+    if ((rc = fork_side(*ss, st))) return rc;
     if ((rc = cuda_rc((vh ? launch_bwd_dhidden_vh : launch_bwd_dhidden)(mDlK.m, mWDh.m, s5, e5,
                                                                         st))))
       return rc;
@@ -936,7 +996,7 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     // dweight (+)= hidden[n0 : n0 + rows]^T @ dlogits ([H,V]) or its transpose ([V,H])
     GemmShape s4 = vh ? base_shape(L2_NORMAL, L2_EVICT_LAST) : base_shape(L2_EVICT_LAST, L2_NORMAL);
     s4.k_blocks = static_cast<int>(cdiv(rows, BK));
-    s4.sched = sched_counters(err);
+    s4.sched = sched_counters(err, 1);
     EpiArgs e4{};
     e4.V = V;
     e4.err = err;
@@ -965,15 +1025,16 @@ int flce_forward_backward(const flce_params* p, const void* hidden, const void* 
     if (L.chunks == 1) {
       e4.out = static_cast<__nv_bfloat16*>(dweight);
       e4.ld_out = ld_dw;
-      rc = cuda_rc(launch_bwd_dweight(a4.m, b4.m, s4, e4, st));
+      rc = cuda_rc(launch_bwd_dweight(a4.m, b4.m, s4, e4, ss->stream));
     } else {
       e4.acc = dwacc;
       e4.acc_out = static_cast<__nv_bfloat16*>(dweight);
       e4.ld_acc = ld_dw;
       e4.acc_mode = c == 0 ? ACC_FIRST : c == L.chunks - 1 ? ACC_LAST : ACC_MID;
-      rc = cuda_rc(launch_bwd_dweight_acc(a4.m, b4.m, s4, e4, st));
+      rc = cuda_rc(launch_bwd_dweight_acc(a4.m, b4.m, s4, e4, ss->stream));
     }
     if (rc) return rc;
+    if ((rc = join_side(*ss, st))) return rc;
   }
   if (!per_token) {
     reduce_rows_kernel<<<1, 1024, 0, st>>>(loss_row, ent_row, labels, N, p->ignore_index,

@@ -331,7 +331,7 @@ int main(void) {
 
 def test_auto_chunking_follows_the_documented_rules(lib):
     """flce.h: the backward's chunk_v = 0 picks the widest multiple of 256 columns whose bf16
-    dlogits [N, chunk_v] fit 1 GiB; flce_forward_backward's chunk_n = 0 the largest multiple
+    dlogits [N, chunk_v] fit 2 GiB; flce_forward_backward's chunk_n = 0 the largest multiple
     of 512 rows whose fp32 logits and bf16 dlogits (V rounded up to 256) fit 8 GiB.  Checked
     through the launch counts (3 GEMMs per vocabulary chunk, 6 launches per token chunk)."""
     import random
@@ -340,7 +340,7 @@ def test_auto_chunking_follows_the_documented_rules(lib):
     for _ in range(200):
         N = rng.choice([1, 7, 300, 4096, 8192, 16384, 65536, 200000])
         V = 8 * rng.randint(1, 40000)
-        vc = max(256, min((1 << 30) // (2 * N) // 256 * 256, cdiv(V, 256) * 256))
+        vc = max(256, min((2 << 30) // (2 * N) // 256 * 256, cdiv(V, 256) * 256))
         p = flce.make_params(N, 64, V, "none")
         assert flce.kernel_launches(p, 1) == 1 + 3 * cdiv(V, vc), (N, V)
         ldz = cdiv(V, 256) * 256

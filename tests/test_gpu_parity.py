@@ -331,10 +331,11 @@ def test_binding_rejects_mismatched_outputs_and_workspace():
 
 
 def test_schedule_counters_are_zero_after_every_call():
-    """The GEMMs draw their tiles from two counters in the workspace header (bytes
-    128-135); the last CTA pair of each GEMM resets them, so after a call that ran many
-    GEMMs on one workspace (a backward of four vocabulary chunks: 12 GEMMs; a gradient-
-    in-forward call of three token chunks: 9) they are zero again, and results are right."""
+    """The GEMMs draw their tiles from pairs of counters in the workspace header (bytes
+    128-135 for the caller's stream, 136-143 for dweight running beside dhidden); the last
+    CTA pair of each GEMM resets its pair, so after a call that ran many GEMMs on one
+    workspace (a backward of four vocabulary chunks: 12 GEMMs; a gradient-in-forward call
+    of three token chunks: 9) they are zero again, and results are right."""
     _cuda_or_skip()
     from linear_cross_entropy_forward_gb300 import (flce_forward_backward, make_params,
                                                     workspace_size)
@@ -357,7 +358,7 @@ def test_schedule_counters_are_zero_after_every_call():
                                     workspace=ws_g)
         torch.cuda.synchronize()
         for ws in (ws_f, ws_b, ws_g):
-            assert torch.all(ws[128:136] == 0), ws[128:136].tolist()
+            assert torch.all(ws[128:144] == 0), ws[128:144].tolist()
     o, dh_o, dw_o = oracle_run(w, hidden, weight, labels, g_loss, g_ent)
     f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
     assert rel_l2(f(dh), dh_o) <= GRAD_REL_L2 and rel_l2(f(dw), dw_o) <= GRAD_REL_L2

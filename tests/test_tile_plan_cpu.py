@@ -27,7 +27,8 @@ CASES = [
     # 2 MiB: 20 fit 40 MiB, fewer than the 32 M tiles but not fewer than the square
     # side 8 -> group 20, hints kept.
     ("llama3_forward", (32, 501, 0, 2 * MiB, EVICT_LAST, NORMAL), (20, EVICT_LAST, NORMAL)),
-    # Llama-3 dlogits, first 65536-column chunk: 32 x 256 tiles, same panels -> 20.
+    # Llama-3-shaped dlogits over a 65536-column vocabulary chunk: 32 x 256 tiles, same
+    # panels -> 20.
     ("llama3_dlogits", (32, 256, 0, 2 * MiB, EVICT_LAST, NORMAL), (20, EVICT_LAST, NORMAL)),
     # Llama-3 dweight [H,V], first chunk: 16 x 256 tiles, hidden^T panels 256 x 8192 x
     # 2 B = 4 MiB: 10 fit, >= 8 -> group 10, hints kept.
