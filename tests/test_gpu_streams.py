@@ -1,0 +1,110 @@
+"""The backward's side stream: dweight runs beside dhidden on an internal stream forked from
+the caller's stream and joined back before the call returns.  Results must not depend on
+which stream the caller uses, work the caller enqueues after the call must see the
+finished gradients, and concurrent calls from two host threads on their own streams (each
+thread has its own side stream) must each be right."""
+import dataclasses
+import threading
+
+import pytest
+import torch
+
+from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward,
+                                                flce_forward_backward)
+from linear_cross_entropy_forward_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+W = dataclasses.replace(wl.TINY, name="st", N=1100, H=200, V=1000, reduction="none",
+                        grad_mode="normal", zloss_coef=1e-3)
+
+
+def _cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_cross_entropy_forward_gb300.build import build
+    build()
+
+
+def _inputs(seed=0):
+    w = dataclasses.replace(W, seed=seed)
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
+    dev = torch.device("cuda")
+    return (hidden.to(dev), weight.to(dev), labels.to(dev), g_loss.to(dev), g_ent.to(dev))
+
+
+def _two_call(hd, Wd, yd, gl, ge, chunk_v):
+    _, _, lse, ez = flce_forward(hd, Wd, yd, "none", zloss_coef=1e-3, validate=True)
+    return flce_backward(hd, Wd, yd, lse, ez, gl, ge, "none", zloss_coef=1e-3, validate=True,
+                         chunk_v=chunk_v)
+
+
+def _bits(t):
+    return t.view(torch.int16)
+
+
+@pytest.mark.parametrize("chunk_v", [0, 256])
+def test_user_stream_gives_the_default_streams_bits(chunk_v):
+    _cuda_or_skip()
+    hd, Wd, yd, gl, ge = _inputs()
+    ref = _two_call(hd, Wd, yd, gl, ge, chunk_v)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dh, dw = _two_call(hd, Wd, yd, gl, ge, chunk_v)
+        # enqueued after the call on the same stream: must see the finished gradients
+        dw_copy = dw.clone()
+        dh_copy = dh.clone()
+    s.synchronize()
+    assert torch.equal(_bits(dh), _bits(ref[0])) and torch.equal(_bits(dw), _bits(ref[1]))
+    assert torch.equal(_bits(dh_copy), _bits(ref[0]))
+    assert torch.equal(_bits(dw_copy), _bits(ref[1]))
+
+
+def test_gradient_in_forward_on_a_user_stream():
+    _cuda_or_skip()
+    hd, Wd, yd, gl, ge = _inputs()
+    ref = flce_forward_backward(hd, Wd, yd, gl, ge, "none", zloss_coef=1e-3, chunk_n=512)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = flce_forward_backward(hd, Wd, yd, gl, ge, "none", zloss_coef=1e-3, chunk_n=512)
+        dw_copy = out[5].clone()
+    s.synchronize()
+    assert torch.equal(_bits(out[4]), _bits(ref[4])) and torch.equal(_bits(out[5]), _bits(ref[5]))
+    assert torch.equal(_bits(dw_copy), _bits(ref[5]))
+
+
+def test_two_host_threads_on_their_own_streams():
+    _cuda_or_skip()
+    inputs = [_inputs(seed) for seed in (0, 1)]
+    refs = []
+    for args in inputs:
+        refs.append(_two_call(*args, chunk_v=256))
+    torch.cuda.synchronize()
+    results = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                outs = []
+                for _ in range(3):
+                    outs.append(_two_call(*inputs[i], chunk_v=256))
+            s.synchronize()
+            results[i] = outs
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for i in range(2):
+        for dh, dw in results[i]:
+            assert torch.equal(_bits(dh), _bits(refs[i][0]))
+            assert torch.equal(_bits(dw), _bits(refs[i][1]))
