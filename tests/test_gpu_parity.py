@@ -131,6 +131,12 @@ CASES = [
     ("one_row", dataclasses.replace(W0, name="t2", N=1, H=8, V=8, ignore_frac=0.0), 0),
     ("big_logits", dataclasses.replace(W0, name="t3", N=200, H=512, V=1024, w_std=0.5,
                                        reduction="none", grad_mode="normal"), 0),
+    # vocabularies wider than 65536 columns at small N: one backward chunk of 70000
+    # columns, and two chunks of 70144 columns (fp32 accumulation of dhidden across them)
+    ("dhidden_split", dataclasses.replace(W0, name="d7", N=300, H=64, V=70000,
+                                          reduction="none", grad_mode="normal"), 0),
+    ("dhidden_split_chunks", dataclasses.replace(W0, name="d8", N=130, H=72, V=140000,
+                                                 zloss_coef=1e-3), 70144),
 ]
 
 

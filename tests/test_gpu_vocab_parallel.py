@@ -126,14 +126,15 @@ def test_single_rank_wrapper_matches_unsharded_path():
     assert rel_l2(W.grad.float().cpu().numpy(), dw.float().cpu().numpy()) <= 1e-3
 
 
-@pytest.mark.parametrize("chunk_v", [0, 256])
-def test_fp32_dhidden_rounds_to_the_bf16_dhidden(chunk_v):
+@pytest.mark.parametrize("V,chunk_v", [(1000, 0), (1000, 256), (70000, 0)])
+def test_fp32_dhidden_rounds_to_the_bf16_dhidden(V, chunk_v):
     """dhidden_fp32 returns the fp32 accumulation the bf16 output is rounded from: one
-    vocabulary chunk (the tile's accumulator) or several (the fp32 sum over chunks), the
-    same sums in the same order, so rounding it gives the bf16 output's bits."""
+    vocabulary chunk (the tile's accumulator, also over a 70000-column k-loop) or several
+    (the fp32 sum over chunks), the same sums in the same order, so rounding it gives the
+    bf16 output's bits."""
     _cuda_or_skip()
     dev = torch.device("cuda")
-    w = dataclasses.replace(wl.TINY, name="vp7", N=300, H=136, V=1000, zloss_coef=1e-3,
+    w = dataclasses.replace(wl.TINY, name="vp7", N=300, H=136, V=V, zloss_coef=1e-3,
                             softcap=8.0)
     hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
     hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
