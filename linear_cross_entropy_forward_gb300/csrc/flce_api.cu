@@ -9,14 +9,17 @@
 //   3. reduce (mean/sum only): fixed-order fp64 sum over rows.
 // Backward, per vocabulary chunk of width Vc (after a per-row prep kernel):
 //   4. bwd_dlogits GEMM: recompute logits, write dlogits[N, Vc] (bf16).
-//   5. bwd_dweight GEMM: dweight[:, chunk] = hidden^T @ dlogits.
-//   6. bwd_dhidden GEMM: dhidden (fp32 accumulator) += dlogits @ weight[:, chunk]^T;
+//   5. bwd_dhidden GEMM: dhidden (fp32 accumulator) += dlogits @ weight[:, chunk]^T;
 //      the last chunk writes bf16.
+//   6. bwd_dweight GEMM, beside dhidden on a side stream: dweight[:, chunk] =
+//      hidden^T @ dlogits.
 // Forward + backward in one call (gradient in forward), per chunk of tokens:
 //   1. fwd_stats GEMM that also keeps the raw fp32 logits of the chunk,
 //   2. combine, prep, then dlogits from the kept logits (no recompute),
-//   3. dhidden rows of the chunk = dlogits @ weight^T (all of V in one GEMM),
-//   4. dweight = hidden^T @ dlogits, written once (one chunk) or accumulated.
+//   3. dhidden rows of the chunk = dlogits @ weight^T (all of V in one GEMM), and
+//      beside it on the side stream dweight = hidden^T @ dlogits, written once (one
+//      chunk) or accumulated.
+// Every GEMM hands its tiles out dynamically from counters in the workspace header.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -446,7 +449,7 @@ int flce_kernel_launches(const flce_params* p, int phase) {
   switch (phase) {
     case 0:  // flce_forward: GEMM, [class-weight sum], combine, [reduce]
       return 2 + reduce + (p->label_smoothing != 0.0f && p->class_weight ? 1 : 0);
-    case 1:  // flce_backward: prep + 3 GEMMs per vocabulary chunk
+    case 1:  // flce_backward: prep + 3 GEMMs (dlogits, dhidden, dweight) per vocabulary chunk
       return 1 + 3 * static_cast<int>(bwd_layout(p).chunks);
     case 2:  // flce_combine_shards: combine, [reduce]
       return 1 + reduce;
