@@ -3,7 +3,8 @@ and random combinations of every option -- reduction, z-loss, soft-cap, label
 smoothing, class weights, weight layout, backward vocabulary chunk, token chunk, and
 the two-call vs gradient-in-forward path -- against the fp64 oracle, with the stated
 tolerances (per-token abs <= 2e-3, reduced rel <= 1e-4, gradients rel-L2 <= 1e-2,
-ignored rows exactly zero)."""
+ignored rows exactly zero).  A second set adds the options of the C ABI's later
+version: a [V,H] weight with any vocabulary size, and an fp32 dhidden."""
 import dataclasses
 import random
 
@@ -65,12 +66,35 @@ def random_case(i):
 
 
 CASES = [random_case(i) for i in range(N_CASES)]
+N_CASES2 = 16
+
+
+def random_case_v2(i):
+    """[V,H] weights with any vocabulary size (not a multiple of 8) and fp32 dhidden,
+    with the other options drawn as above."""
+    w, o = random_case(100 + i)
+    r = random.Random(5000 + i)
+    o = dict(o, layout="vh", dh32=r.random() < 0.6)
+    w = dataclasses.replace(w, name=f"rand2_{i}", V=r.randint(1, 4000))
+    return w, o
+
+
+CASES2 = [random_case_v2(i) for i in range(N_CASES2)]
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_case_matches_oracle(i):
     _cuda_or_skip()
-    w, o = CASES[i]
+    check_case(i, *CASES[i])
+
+
+@pytest.mark.parametrize("i", range(N_CASES2))
+def test_random_case_any_vocabulary_and_fp32_dhidden(i):
+    _cuda_or_skip()
+    check_case(1000 + i, *CASES2[i])
+
+
+def check_case(i, w, o):
     hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
     cw = None
     if o["class_weight"]:
@@ -89,13 +113,16 @@ def test_random_case_matches_oracle(i):
     Wd = weight.to(dev) if o["layout"] == "hv" else weight.t().contiguous().to(dev)
     kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=o["layout"],
               label_smoothing=o["eps"], class_weight=None if cw is None else cw.to(dev))
+    dh32 = o.get("dh32", False)
     if o["fused"]:
         loss, ent, lse, ez, dh, dw = flce_forward_backward(
-            hd, Wd, yd, gl, ge, w.reduction, validate=True, chunk_n=o["chunk_n"], **kw)
+            hd, Wd, yd, gl, ge, w.reduction, validate=True, chunk_n=o["chunk_n"],
+            dhidden_fp32=dh32, **kw)
     else:
         loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True, **kw)
         dh, dw = flce_backward(hd, Wd, yd, lse, ez, gl, ge, w.reduction, validate=True,
-                               chunk_v=o["chunk_v"], **kw)
+                               chunk_v=o["chunk_v"], dhidden_fp32=dh32, **kw)
+    assert dh.dtype == (torch.float32 if dh32 else torch.bfloat16)
     torch.cuda.synchronize()
     if o["layout"] == "vh":
         dw = dw.t()
@@ -117,5 +144,6 @@ def test_random_case_matches_oracle(i):
         else:  # every row ignored (or zero upstream gradients): exactly zero
             assert np.all(got == 0), desc
     ign = np.nonzero(~valid)[0]
-    if ign.size:
-        assert torch.all(dh.cpu()[torch.from_numpy(ign)].view(torch.int16) == 0), desc
+    if ign.size:  # bitwise zero (no -0.0 either)
+        bits = dh.cpu()[torch.from_numpy(ign)].view(torch.int32 if dh32 else torch.int16)
+        assert torch.all(bits == 0), desc
