@@ -256,8 +256,8 @@ const char* flce_strerror(int code);
  *   held by every GPU that loads the library until the process exits; problems
  *   whose flce_workspace_size(params, 0) exceeds it return FLCE_ERR_SCRATCH_LIMIT
  *   without enqueueing anything.  Nothing is allocated (no cudaMalloc/cudaFree).
- *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.  All calls
+ *   The first call on a device looks up the array's device address (once, with
+ *   that device current, through the runtime's symbol lookup).  All calls
  *   share the array (its header is cleared on every call; the rest is fully
  *   rewritten), so calls that may overlap on the GPU -- other streams, other
  *   threads -- race and must be serialised by the caller.  flce_status() is not
