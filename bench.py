@@ -18,7 +18,9 @@ baseline arm), on bounded row samples of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -47,7 +49,9 @@ def parse_args():
                     help="reduced case: replace the workload's N (for small ncu captures)")
     ap.add_argument("--vocab", type=int, default=0,
                     help="reduced case: replace the workload's V (for small ncu captures)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--softcap", type=float, default=None,
+                    help="reduced case: replace the workload's logit soft-cap (0 = none)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused-memory", action="store_true",
                     help="skip the unfused PyTorch baseline (its peak memory and its time)")
@@ -119,6 +123,8 @@ def select_workload(args):
         N = args.tokens or w.N
         V = args.vocab or w.V
         w = w.scaled(f"{w.name}_N{N}_V{V}", N, w.H, V)
+    if args.softcap is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_cap{args.softcap:g}", softcap=args.softcap)
     return w
 
 
@@ -148,17 +154,25 @@ def oracle_inputs(w, hidden, weight, labels, g_loss, g_ent):
 
 
 def calibrate_rows(w, args_oracle, seconds):
-    """Rows per oracle sample so that one sample takes about `seconds` (the cost grows
-    linearly with the rows once the sample is long enough to amortise set-up)."""
-    rows = 4
+    """Rows per oracle sample so that one sample takes about `seconds`.  A sample costs a
+    fixed set-up plus a cost per row, so the last two trial samples (4x apart in rows)
+    give the line a + b * rows that the row count is read from."""
+    rows, trials = 4, []
     while True:
         t0 = time.perf_counter()
         oracle_sample_step(w, *args_oracle, rows=rows)
-        t = max(time.perf_counter() - t0, 1e-3)
-        if t >= 0.1 * seconds or rows >= w.N:
+        trials.append((rows, max(time.perf_counter() - t0, 1e-3)))
+        if trials[-1][1] >= 0.1 * seconds or rows >= w.N:
             break
         rows = min(w.N, rows * 4)
-    return max(1, min(w.N, int(rows * seconds / t))), t
+    r1, t1 = trials[-1]
+    b = t1 / r1
+    if len(trials) > 1:
+        r0, t0_ = trials[-2]
+        if t1 > t0_ and r1 > r0:
+            b = (t1 - t0_) / (r1 - r0)
+    a = max(0.0, t1 - b * r1)
+    return max(1, min(w.N, int((seconds - a) / b))), t1
 
 
 def cpu_baseline(w, hidden, weight, labels, g_loss, g_ent, seconds):
@@ -368,9 +382,10 @@ def unfused_baseline(torch, w, hd, Wd, yd, gld, ged, dev, warmup=2, steps=3):
                     "entropy, cross-entropy, autograd backward), masked like the fused path"}
 
 
-def time_other_workload(torch, w, steps, warmup, dev, local):
+def time_other_workload(torch, w, steps, warmup, dev, local, min_seconds=1.0):
     """The two-call step (flce_forward + flce_backward) of another workload: the same
-    timing and clock sampling as the headline line's, nothing else."""
+    timing and clock sampling as the headline line's (the forward call timed apart too),
+    over at least `steps` steps and at least `min_seconds` of them."""
     from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward, make_params,
                                                     workspace_size)
     from linear_cross_entropy_forward_gb300.workloads import make_inputs
@@ -391,35 +406,50 @@ def time_other_workload(torch, w, steps, warmup, dev, local):
     kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if needs_flush(w) else None
 
-    def step():
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         flce_forward(hd, Wd, yd, w.reduction, workspace=ws_f, out=out_f, **kw)
+        if ev is not None:
+            ev[1].record(stream)
         flce_backward(hd, Wd, yd, out_f[2], out_f[3], gld, ged, w.reduction, workspace=ws_b,
                       out=out_b, **kw)
+        if ev is not None:
+            ev[2].record(stream)
 
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(warmup):
         step()
+    w1.record(stream)
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
+    # at least min_seconds of timed steps, so that the clock record holds several samples
+    # under load (a short workload's K steps alone take a fraction of a sampling period)
+    est = w0.elapsed_time(w1) / max(warmup, 1)
+    steps = max(steps, min(20000, math.ceil(min_seconds * 1e3 / max(est, 1e-3))))
     sampler = ClockSampler(nvsmi_id(torch, local))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     t0 = time.time()
     for i in range(steps):
         if flush is not None:
             flush.fill_(i & 255)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+        step(ev[i])
     torch.cuda.synchronize()
     t1 = time.time()
     sampler.stop()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    ms = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+    f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     tflops = 8.0 * N * H * V / (ms / 1e3) / 1e12
+    f_tflops = 2.0 * N * H * V / (f_ms / 1e3) / 1e12
     peak, _ = load_peaks()
     clocks = sampler.summary(t0, t1)
     res = {"N": N, "H": H, "V": V, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
-           "tflops": tflops, "frac_of_peak": tflops / peak, "clocks": clocks,
-           "steps": steps, "warmup": warmup,
+           "tflops": tflops, "frac_of_peak": tflops / peak,
+           "fwd_ms": f_ms, "fwd_tflops": f_tflops, "fwd_frac_of_peak": f_tflops / peak,
+           "clocks": clocks, "steps": steps, "warmup": warmup,
            "l2": "flushed between steps" if flush is not None else "inputs larger than L2"}
     del hd, Wd, yd, out_f, out_b, ws_f, ws_b, flush
     torch.cuda.empty_cache()
@@ -593,6 +623,8 @@ def run_ours(args):
             pg.barrier()
         steps = args.e2e_steps
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        sampler = ClockSampler(nvsmi_id(torch, local))
+        t0 = time.time()
         ev[0].record(stream)
         pipe.copy_stream.wait_stream(stream)
         pipe.submit(*host_in)
@@ -602,13 +634,15 @@ def run_ours(args):
             pipe.step()
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
+        t1 = time.time()
+        sampler.stop()
         ms = ev[0].elapsed_time(ev[steps]) / steps
         med = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
         if pg:
             t = torch.tensor([ms], device=dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             ms = float(t.item())
-        res = (ms, med, pipe.h2d_bytes(), pipe.d2h_bytes())
+        res = (ms, med, pipe.h2d_bytes(), pipe.d2h_bytes(), sampler.summary(t0, t1))
         del pipe
         return res
 
@@ -616,9 +650,9 @@ def run_ours(args):
     if not args.no_e2e:
         e2e_res = e2e(False)
         if gif is not None:
-            gms, gmed, _, _ = e2e(True)
+            gms, gmed, _, _, gclk = e2e(True)
             gif["e2e"] = {"value": N * world / (gms / 1e3), "unit": UNIT, "ms_per_step": gms,
-                          "median_step_ms": gmed}
+                          "median_step_ms": gmed, "clocks": gclk}
 
     # the unfused baseline: the pages' equivalent compute logic in plain PyTorch (fp32
     # logits, softmax, entropy, cross-entropy, autograd backward), run outside every
@@ -670,10 +704,12 @@ def run_ours(args):
         "clocks": clocks,
     }
     if e2e_res is not None:
-        e2e_ms, e2e_med, h2d, d2h = e2e_res
+        e2e_ms, e2e_med, h2d, d2h, e2e_clk = e2e_res
+        # its own window's clock record: under the power cap the clock settles a little
+        # differently from one window to the next, so compare the two per clock
         out["e2e"] = {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                      "median_step_ms": e2e_med}
+                      "median_step_ms": e2e_med, "clocks": e2e_clk}
     if unfused is not None:
         unfused["speedup_of_fused"] = unfused["ms_per_step"] / ms_step
         out["unfused_baseline"] = unfused
@@ -682,7 +718,8 @@ def run_ours(args):
         out["grad_in_forward"] = gif
     if gif is not None:
         out["memory"]["grad_in_forward_extra_bytes"] = gif["workspace_bytes"]
-    if not args.no_other_workloads and not (args.tokens or args.vocab):
+    reduced = args.tokens or args.vocab or args.softcap is not None
+    if world == 1 and not args.no_other_workloads and not reduced:
         # the other workloads' two-call step, measured the same way (no e2e, no baselines)
         from linear_cross_entropy_forward_gb300.workloads import WORKLOADS
         others = {}
@@ -691,6 +728,7 @@ def run_ours(args):
                 continue
             others[name] = time_other_workload(torch, ow, args.steps, args.warmup, dev, local)
         out["other_workloads"] = others
+    if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
                                            args.cpu_seconds)
     if rank == 0:
