@@ -41,7 +41,8 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
  *     enqueued asynchronously on it; nothing synchronises unless params->validate
  *     is set.  The backward passes run their dweight GEMM beside dhidden on an
- *     internal stream (one per host thread and device, created on first use) that
+ *     internal stream (one per host thread and device, created on first use and
+ *     destroyed when the thread exits) that
  *     is forked from `stream` by an event and joined back before the call returns,
  *     so every call's work still follows the work enqueued on `stream` before it and
  *     precedes the work enqueued after it.

@@ -289,10 +289,14 @@ int device_info(DevInfo* out) {
   return FLCE_OK;
 }
 
+// The error word is copied on `st` itself, after the call's work, so that reading it
+// waits for nothing but that stream (a plain cudaMemcpy would also wait for the legacy
+// default stream).
 int read_status(const void* workspace, cudaStream_t st) {
   uint32_t word = 0;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
-  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
     return FLCE_ERR_CUDA;
   if (word & FLCE_DEVERR_BOUNDS) return FLCE_ERR_BOUNDS;
   if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
@@ -310,17 +314,32 @@ inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR
 // dynamic tile schedule balances the work between them.  The side stream and its two
 // events are created once per host thread and device: events are never shared between
 // threads, and a stream wait binds to the record before it, so reusing them across one
-// thread's calls is safe.
+// thread's calls is safe.  They are destroyed when the thread exits (destroying a stream
+// or an event with work still pending is allowed: the work completes first).
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 
+struct SideStreams {
+  SideStream per_device[64];
+  ~SideStreams() {
+    for (SideStream& ss : per_device) {
+      if (!ss.stream) continue;
+      // at process exit the runtime may already be unloaded: the calls then fail
+      // harmlessly
+      cudaEventDestroy(ss.fork);
+      cudaEventDestroy(ss.join);
+      cudaStreamDestroy(ss.stream);
+    }
+  }
+};
+
 int side_stream(SideStream** out) {
-  thread_local SideStream cache[64];
+  thread_local SideStreams cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FLCE_ERR_CUDA;
-  SideStream& ss = cache[dev];
+  SideStream& ss = cache.per_device[dev];
   if (!ss.stream) {
     SideStream n;
     if (cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking) != cudaSuccess)

@@ -108,3 +108,35 @@ def test_two_host_threads_on_their_own_streams():
         for dh, dw in results[i]:
             assert torch.equal(_bits(dh), _bits(refs[i][0]))
             assert torch.equal(_bits(dw), _bits(refs[i][1]))
+
+
+def test_thread_exit_with_the_backward_still_running():
+    """A host thread that enqueues a backward and exits at once: its side stream and
+    events are destroyed at thread exit while dweight may still be running on them,
+    which must neither lose nor reorder work."""
+    _cuda_or_skip()
+    args = _inputs(0)
+    ref = _two_call(*args, chunk_v=256)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        box = {}
+
+        def work():
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            hd, Wd, yd, gl, ge = args
+            with torch.cuda.stream(s):
+                # without validate nothing waits for the stream before the thread ends
+                _, _, lse, ez = flce_forward(hd, Wd, yd, "none", zloss_coef=1e-3)
+                box["out"] = flce_backward(hd, Wd, yd, lse, ez, gl, ge, "none",
+                                           zloss_coef=1e-3, chunk_v=256)
+            box["stream"] = s
+
+        t = threading.Thread(target=work)
+        t.start()
+        t.join(timeout=120)
+        assert "out" in box
+        box["stream"].synchronize()
+        dh, dw = box["out"]
+        assert torch.equal(_bits(dh), _bits(ref[0]))
+        assert torch.equal(_bits(dw), _bits(ref[1]))
