@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import _fullsize_oracle as fso
-from linear_cross_entropy_forward_gb300 import flce_backward, flce_forward
+from linear_cross_entropy_forward_gb300 import (flce_backward, flce_forward,
+                                                flce_forward_backward)
 from linear_cross_entropy_forward_gb300 import workloads as wl
 from oracle import flce_oracle as orc
 
@@ -169,3 +170,52 @@ def test_fullsize_weight_layouts_agree_bitwise():
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
         else:
             assert torch.equal(a, b)
+
+
+def test_qwen_batch_with_arrays_past_2_31_elements():
+    """Qwen2.5 RL batch (N = 16384, V = 152064) with the whole problem in one chunk: the
+    backward's dlogits chunk of all 152064 columns and the gradient-in-forward call's kept
+    logits of all 16384 rows each hold 2.49e9 elements (5.0 and 10.0 GB), more than 2^31,
+    so the epilogue stores, the TMA maps over these arrays and dlogits_from_z all index
+    past it.  dweight does not depend on the vocabulary chunking (every column sums over
+    the rows in the same order): bitwise that of the default chunks.  The two one-chunk
+    runs form the same dlogits and contract them the same way, so they agree bit for bit.
+    dhidden rows and dweight columns against the oracle."""
+    _cuda_or_skip()
+    w = wl.QWEN25
+    assert w.N * w.V > 2 ** 31 and w.V % 256 == 0 and w.N % 512 == 0
+    dev = torch.device("cuda")
+    hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w, label_device="cuda")
+    hd, Wd, yd = hidden.to(dev), weight.to(dev), labels.to(dev)
+    gl, ge = g_loss.to(dev), g_ent.to(dev)
+    kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap)
+    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, validate=True, **kw)
+    _, dw_d = flce_backward(hd, Wd, yd, lse, ez, gl, ge, w.reduction, validate=True, **kw)
+    dh_1, dw_1 = flce_backward(hd, Wd, yd, lse, ez, gl, ge, w.reduction, validate=True,
+                               chunk_v=w.V, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(dw_1.view(torch.int16), dw_d.view(torch.int16))
+    del dw_d
+    torch.cuda.empty_cache()
+    out = flce_forward_backward(hd, Wd, yd, gl, ge, w.reduction, validate=True, chunk_n=w.N,
+                                **kw)
+    torch.cuda.synchronize()
+    for a, b in zip(out[:4], (loss, ent, lse, ez)):
+        assert torch.equal(a, b)
+    assert torch.equal(out[4].view(torch.int16), dh_1.view(torch.int16))
+    assert torch.equal(out[5].view(torch.int16), dw_1.view(torch.int16))
+    del out
+    torch.cuda.empty_cache()
+
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    o, h64, W64, _ = oracle_whole_batch(w, hidden, weight, labels, "none", **kw)
+    assert np.abs(f64(lse) - o["lse"]).max() <= TOK_ABS
+    y = labels.cpu().numpy()
+    rows = sample_rows(w, labels.cpu())
+    dh_o, _ = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.cpu().numpy(),
+                           g_ent.cpu().numpy(), w.reduction, rows=rows, **kw)
+    assert rel_l2(f64(dh_1[torch.from_numpy(rows).to(dev)]), dh_o) <= GRAD_REL_L2
+    cols = fso.dweight_columns(w.V, y)
+    _, dw_o = orc.backward(h64, W64, y, o["lse"], o["ez"], g_loss.cpu().numpy(),
+                           g_ent.cpu().numpy(), w.reduction, cols=cols, **kw)
+    assert rel_l2(f64(dw_1[:, torch.from_numpy(cols).to(dev)]), dw_o) <= GRAD_REL_L2

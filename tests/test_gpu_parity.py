@@ -137,6 +137,10 @@ CASES = [
                                           reduction="none", grad_mode="normal"), 0),
     ("dhidden_split_chunks", dataclasses.replace(W0, name="d8", N=130, H=72, V=140000,
                                                  zloss_coef=1e-3), 70144),
+    # a vocabulary of two million columns and a ragged last tile: 8194 tiles per row of
+    # forward partials to merge, column indices past 2^21 in every kernel
+    ("vocab_2m", dataclasses.replace(W0, name="v2m", N=130, H=64, V=2 ** 21 + 264,
+                                     zloss_coef=1e-3), 0),
 ]
 
 
