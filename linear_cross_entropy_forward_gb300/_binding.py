@@ -13,7 +13,7 @@ import threading
 
 import torch
 
-from .workloads import IGNORE_INDEX, RED_MEAN, RED_NONE, RED_SUM, reduction_code
+from .workloads import IGNORE_INDEX, RED_NONE, reduction_code
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG_DIR, "libflce.so")
