@@ -176,14 +176,31 @@ def calibrate_rows(w, args_oracle, seconds):
 
 
 def cpu_baseline(w, hidden, weight, labels, g_loss, g_ent, seconds):
+    """The oracle timed on a row sample; also returns its forward outputs for those rows,
+    which the bench line compares with the GPU's."""
     ai = oracle_inputs(w, hidden, weight, labels, g_loss, g_ent)
     rows, _ = calibrate_rows(w, ai, seconds)
     t0 = time.perf_counter()
-    oracle_sample_step(w, *ai, rows=rows)
+    o = oracle_sample_step(w, *ai, rows=rows)
     dt = time.perf_counter() - t0
     return {"value": rows / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": f"fp64 numpy oracle fwd+bwd on the first {rows} of {w.N} rows "
-                      f"(full H={w.H}, V={w.V}), {dt:.1f} s on {blas_threads()} BLAS threads"}
+                      f"(full H={w.H}, V={w.V}), {dt:.1f} s on {blas_threads()} BLAS threads"}, o
+
+
+def oracle_check(o, lse, ez, loss, ent, reduction):
+    """Max abs error of the GPU's per-row outputs of the timed runs against the oracle's
+    on the CPU-baseline sample (the tolerance of the parity tests: 2e-3)."""
+    import numpy as np
+    r = len(o["lse"])
+    f64 = lambda t: t[:r].float().cpu().numpy().astype(np.float64)  # noqa: E731
+    errs = {"lse": float(np.abs(f64(lse) - o["lse"]).max()),
+            "ez": float(np.abs(f64(ez) - o["ez"]).max())}
+    if reduction == "none":
+        errs["loss"] = float(np.abs(f64(loss) - o["loss"]).max())
+        errs["entropy"] = float(np.abs(f64(ent) - o["entropy"]).max())
+    return {"rows": r, "max_abs_err": errs, "tolerance_abs": 2e-3,
+            "pass": all(e <= 2e-3 for e in errs.values())}
 
 
 # ---------------------------------------------------------------- clocks sampler
@@ -729,8 +746,10 @@ def run_ours(args):
             others[name] = time_other_workload(torch, ow, args.steps, args.warmup, dev, local)
         out["other_workloads"] = others
     if world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
-                                           args.cpu_seconds)
+        out["cpu_baseline"], o_sample = cpu_baseline(w, hidden, weight, labels, g_loss, g_ent,
+                                                     args.cpu_seconds)
+        # the outputs of the last timed call against the oracle on the same rows
+        out["oracle_check"] = oracle_check(o_sample, lse, ez, loss, ent, w.reduction)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:

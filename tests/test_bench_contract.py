@@ -103,3 +103,26 @@ def test_reported_peak_is_the_largest_measured_rate():
         return
     peak, _ = bench.load_peaks()
     assert peak == max(v for k, v in t.items() if k.startswith("bf16_tflops"))
+
+
+def test_oracle_check_compares_the_sampled_rows():
+    """bench.py's oracle_check: per-row outputs of the GPU run against the oracle's on the
+    CPU-baseline sample, with the parity tests' 2e-3 absolute tolerance."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    rng = np.random.default_rng(0)
+    o = {k: rng.normal(size=5) for k in ("lse", "ez", "loss", "entropy")}
+    full = {k: torch.tensor(np.concatenate([v, rng.normal(size=3)]), dtype=torch.float32)
+            for k, v in o.items()}
+    res = bench.oracle_check(o, full["lse"], full["ez"], full["loss"], full["entropy"], "none")
+    assert res["rows"] == 5 and res["pass"]
+    assert set(res["max_abs_err"]) == {"lse", "ez", "loss", "entropy"}
+    bad = full["ez"].clone()
+    bad[4] += 0.01  # a sampled row off by more than the tolerance
+    res = bench.oracle_check(o, full["lse"], bad, full["loss"], full["entropy"], "mean")
+    assert not res["pass"] and set(res["max_abs_err"]) == {"lse", "ez"}
+    bad = full["ez"].clone()
+    bad[6] += 1.0  # a row outside the sample is not compared
+    assert bench.oracle_check(o, full["lse"], bad, full["loss"], full["entropy"], "mean")["pass"]
