@@ -64,10 +64,12 @@ __global__ void __launch_bounds__(1024) bwd_prep_kernel(
     int64_t ignore_index, int per_token, int mean, float zcoef, float eps,
     const float* __restrict__ cw, float4* __restrict__ rowc, float* __restrict__ rowd);
 
-__global__ void __launch_bounds__(kDlzThreads) dlogits_from_z_kernel(
-    const float* __restrict__ z, int64_t rows, int64_t ldz, const float4* __restrict__ rowc,
-    const float* __restrict__ rowd, const int64_t* __restrict__ labels, int64_t V,
-    float softcap, int smooth, const float* __restrict__ cw, __nv_bfloat16* __restrict__ dl);
+// dlogits [rows, ldz] bf16 from the kept fp32 logits z [rows, ldz] (rows of two per
+// block; the soft-cap and smoothing variants chosen here).
+cudaError_t launch_dlogits_from_z(const float* z, int64_t rows, int64_t ldz,
+                                  const float4* rowc, const float* rowd, const int64_t* labels,
+                                  int64_t V, float softcap, bool smooth, const float* cw,
+                                  __nv_bfloat16* dl, cudaStream_t st);
 
 __global__ void __launch_bounds__(256) scale_bf16_kernel(__nv_bfloat16* __restrict__ x,
                                                          int64_t n, const float* __restrict__ g);
