@@ -4,8 +4,9 @@ Every row's logsumexp and E_p[z] at a full-size workload cost the oracle a minut
 two of host time (two fp64 passes over all N x V logits).  They depend only on
 hidden, weight and the soft-cap, not on the labels, so they are computed once per
 process and also kept on disk under tests/.oracle_cache/ (git-ignored), keyed by a
-SHA-256 digest of the inputs' bf16 bits, the shapes and the soft-cap.  Everything
-here calls the oracle only; no value comes from the CUDA path.
+SHA-256 digest of the inputs' bf16 bits, the shapes, the soft-cap and the oracle's own
+source (a changed oracle never reads an older entry).  Everything here calls the oracle
+only; no value comes from the CUDA path.
 """
 from __future__ import annotations
 
@@ -20,8 +21,14 @@ CACHE_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), ".oracle_ca
 _memo: dict = {}
 
 
+_ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "oracle", "flce_oracle.py")
+
+
 def _digest(h_bits, w_bits, softcap) -> str:
     d = hashlib.sha256()
+    with open(_ORACLE_SRC, "rb") as f:
+        d.update(f.read())
     for a in (h_bits, w_bits):
         a = np.ascontiguousarray(a)
         d.update(repr((a.shape, a.dtype.str)).encode())
