@@ -126,3 +126,27 @@ def test_oracle_check_compares_the_sampled_rows():
     bad = full["ez"].clone()
     bad[6] += 1.0  # a row outside the sample is not compared
     assert bench.oracle_check(o, full["lse"], bad, full["loss"], full["entropy"], "mean")["pass"]
+
+
+def test_cpu_baseline_sample_is_fitted_to_the_time_budget(monkeypatch):
+    """calibrate_rows reads the row count from a line through its last two trial samples
+    (a fixed set-up cost plus a cost per row), so the timed sample lands on the budget
+    even when the set-up cost is a large part of the trial samples."""
+    sys.path.insert(0, ROOT)
+    import bench
+    clock = [0.0]
+
+    def fake_step(w, *args, rows):
+        clock[0] += 0.8 + 0.02 * rows  # seconds: 0.8 of set-up, 20 ms per row
+
+    monkeypatch.setattr(bench, "oracle_sample_step", fake_step)
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: clock[0])
+
+    class W:
+        N = 8192
+
+    rows, _ = bench.calibrate_rows(W(), (), 15.0)
+    assert rows == int((15.0 - 0.8) / 0.02)
+    # never more rows than the workload has
+    W.N = 100
+    assert bench.calibrate_rows(W(), (), 15.0)[0] == 100
