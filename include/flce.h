@@ -33,7 +33,8 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers to dense row-major arrays, owned by
  *     the caller; the library allocates no device memory and keeps no state
- *     between calls apart from a per-device cache of kernel attributes.
+ *     between calls apart from per-device caches (device attributes, the no-alloc
+ *     scratch address) and the per-thread side streams described below.
  *   - hidden, weight, dhidden, dweight: bf16 (IEEE bfloat16 bit patterns; dhidden fp32
  *     when params->dhidden_fp32 is set); weight and dweight are [H,V] or [V,H] as
  *     params->weight_layout says.
