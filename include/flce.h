@@ -203,6 +203,9 @@ int flce_shard_stats(const flce_params* params, const void* hidden, const void* 
  *   stats: [n_shards, 4, N] fp32, each shard's flce_shard_stats output (as an
  *   all-gather across ranks produces it).  Outputs as flce_forward's, for the whole
  *   vocabulary (params->v_total entries).  workspace: >= flce_workspace_size(params, 2).
+ *   Of params only N, ignore_index, reduction, zloss_coef, validate and v_total are
+ *   used; the shard fields (V, v_offset, weight_layout) need only be a valid shard of
+ *   v_total, e.g. the whole vocabulary as one [V,H] shard, which takes any v_total. 
  * The backward of a shard is flce_backward with the same sharded params and weight
  * slice: it writes that shard's dweight and this shard's term of dhidden, which the
  * caller sums over the shards. */

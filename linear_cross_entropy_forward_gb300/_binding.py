@@ -409,8 +409,10 @@ def flce_combine_shards(stats, labels, v_total, reduction="mean", ignore_index=I
     _need(stats, "stats", torch.float32, (P, 4, N))
     dev = _on_current_device(stats)
     _need(labels, "labels", torch.int64, (N,), dev)
+    # No weight is read here: the parameters describe the whole vocabulary as one
+    # shard, in the [V,H] layout, which puts no alignment rule on its size.
     p = make_params(N, H, v_total, reduction, ignore_index, zloss_coef, 0.0, validate,
-                    v_offset=0, v_total=v_total)
+                    weight_layout=WEIGHT_VH, v_offset=0, v_total=v_total)
     n_out = N if p.reduction == RED_NONE else 1
     loss = torch.empty(n_out, dtype=torch.float32, device=dev)
     ent = torch.empty(n_out, dtype=torch.float32, device=dev)

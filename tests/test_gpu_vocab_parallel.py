@@ -58,6 +58,41 @@ CASES = [
 @pytest.mark.parametrize("name,w,cuts,layout", CASES, ids=[c[0] for c in CASES])
 def test_sequential_shards_match_oracle(name, w, cuts, layout):
     _cuda_or_skip()
+    check_shards(w, cuts, layout)
+
+
+def random_shard_case(i):
+    """Random shapes (ragged in every dimension), 2-8 shards cut at random columns (on
+    the 8-column grid a [H,V] shard's row stride needs; anywhere for [V,H]), and random
+    reduction, z-loss, soft-cap and backward chunk."""
+    import random
+    r = random.Random(7000 + i)
+    layout = r.choice(["hv", "vh"])
+    reduction = r.choice(["none", "mean", "sum"])
+    step = 8 if layout == "hv" else 1
+    P = r.randint(2, 8)
+    V = step * r.randint(P, 3000 // step)
+    cuts = sorted(r.sample(range(1, V // step), P - 1))
+    cuts = [0] + [c * step for c in cuts] + [V]
+    w = dataclasses.replace(
+        wl.TINY, name=f"vprand{i}", seed=300 + i,
+        N=r.choice([1, 37, 255, 300, 513]), H=8 * r.randint(1, 48), V=V,
+        reduction=reduction, ignore_frac=r.choice([0.0, 0.1, 0.5]),
+        zloss_coef=r.choice([0.0, 1e-3]), softcap=r.choice([0.0, 0.0, 5.0]),
+        w_std=r.choice([0.02, 0.2]), grad_mode="normal" if reduction == "none" else "ones")
+    return w, cuts, layout, r.choice([0, 0, 256])
+
+
+RANDOM_CASES = [random_shard_case(i) for i in range(12)]
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_CASES)))
+def test_random_shards_match_oracle(i):
+    _cuda_or_skip()
+    check_shards(*RANDOM_CASES[i])
+
+
+def check_shards(w, cuts, layout, chunk_v=0):
     dev = torch.device("cuda")
     hidden, weight, labels, g_loss, g_ent = wl.make_inputs(w)
     hd, yd = hidden.to(dev), labels.to(dev)
@@ -76,7 +111,7 @@ def test_sequential_shards_match_oracle(name, w, cuts, layout):
         dhp, dwp = flce_backward(hd, ws, yd, lse, ez, g_loss.to(dev), g_ent.to(dev), w.reduction,
                                  zloss_coef=w.zloss_coef, softcap=w.softcap, validate=True,
                                  weight_layout=layout, v_offset=a, v_total=w.V,
-                                 dhidden_fp32=True)
+                                 dhidden_fp32=True, chunk_v=chunk_v)
         assert dhp.dtype == torch.float32
         dh += dhp
         dws.append(dwp if layout == "hv" else dwp.t())
@@ -94,14 +129,18 @@ def test_sequential_shards_match_oracle(name, w, cuts, layout):
     f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
     assert np.abs(f(lse) - o["lse"]).max() <= TOK_ABS
     assert np.abs(f(ez) - o["ez"]).max() <= TOK_ABS
+    desc = f"{w} cuts={cuts} {layout} chunk_v={chunk_v}"
     if w.reduction == "none":
-        assert np.abs(f(loss) - o["loss"]).max() <= TOK_ABS
-        assert np.abs(f(ent) - o["entropy"]).max() <= TOK_ABS
+        assert np.abs(f(loss) - o["loss"]).max() <= TOK_ABS, desc
+        assert np.abs(f(ent) - o["entropy"]).max() <= TOK_ABS, desc
     else:
-        assert abs(loss.item() - o["loss"]) <= RED_REL * abs(o["loss"])
-        assert abs(ent.item() - o["entropy"]) <= RED_REL * abs(o["entropy"])
-    assert rel_l2(f(dh), dh_o) <= GRAD_REL_L2
-    assert rel_l2(f(dw), dw_o) <= GRAD_REL_L2
+        for got, want in ((loss.item(), o["loss"]), (ent.item(), o["entropy"])):
+            assert (abs(got - want) <= RED_REL * abs(want)) if want != 0 else got == 0, desc
+    for got, want in ((f(dh), dh_o), (f(dw), dw_o)):
+        if np.linalg.norm(want) > 0:
+            assert rel_l2(got, want) <= GRAD_REL_L2, desc
+        else:  # every row ignored: exactly zero
+            assert np.all(got == 0), desc
 
 
 def test_single_rank_wrapper_matches_unsharded_path():
