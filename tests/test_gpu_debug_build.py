@@ -6,7 +6,8 @@ FLCE_ERR_BOUNDS.  Every call here runs with validate set, so a bounds failure in
 kernel would raise; the results must also match the fp64 oracle as in the regular
 parity tests.  The cases are ragged in every dimension (N, H and V off the tile
 grid), with several backward vocabulary chunks, token chunks of the gradient-in-
-forward mode, the [V,H] layout with an odd vocabulary, and vocabulary shards.
+forward mode, the [V,H] layout with an odd vocabulary, vocabulary shards, and every case
+of the seeded random sweeps.
 """
 import dataclasses
 
@@ -64,3 +65,16 @@ def test_vocabulary_shards(debug_library):
     import test_gpu_vocab_parallel as tv
     name, w, cuts, layout = tv.CASES[0]
     tv.test_sequential_shards_match_oracle(name, w, cuts, layout)
+
+
+def test_random_sweep_under_bounds_checks(debug_library):
+    """Every case of the seeded random sweeps (C entry points, vocabulary shardings)
+    again, now with every TMA box and epilogue store bounds-checked."""
+    import test_gpu_random_sweep as ts
+    import test_gpu_vocab_parallel as tv
+    for i, (w, o) in enumerate(ts.CASES):
+        ts.check_case(i, w, o)
+    for i, (w, o) in enumerate(ts.CASES2):
+        ts.check_case(1000 + i, w, o)
+    for case in tv.RANDOM_CASES:
+        tv.check_shards(*case)
