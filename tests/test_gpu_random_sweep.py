@@ -4,7 +4,8 @@ smoothing, class weights, weight layout, backward vocabulary chunk, token chunk,
 the two-call vs gradient-in-forward path -- against the fp64 oracle, with the stated
 tolerances (per-token abs <= 2e-3, reduced rel <= 1e-4, gradients rel-L2 <= 1e-2,
 ignored rows exactly zero).  A second set adds the options of the C ABI's later
-version: a [V,H] weight with any vocabulary size, and an fp32 dhidden."""
+version: a [V,H] weight with any vocabulary size, and an fp32 dhidden.  A third set
+takes medium shapes (thousands of tiles per GEMM, several chunks)."""
 import dataclasses
 import random
 
@@ -80,6 +81,23 @@ def random_case_v2(i):
 
 
 CASES2 = [random_case_v2(i) for i in range(N_CASES2)]
+N_CASES3 = 8
+
+
+def random_case_medium(i):
+    """Medium shapes: thousands of output tiles, so every pair of the persistent GEMMs
+    takes many tiles from the dynamic schedule, with several backward vocabulary chunks
+    or token chunks; the other options drawn as above."""
+    w, o = random_case(200 + i)
+    r = random.Random(8000 + i)
+    V = 8 * r.randint(500, 5000) if o["layout"] == "hv" else r.randint(4000, 40000)
+    w = dataclasses.replace(w, name=f"rand3_{i}", N=r.randint(1000, 5000),
+                            H=8 * r.randint(16, 256), V=V)
+    o = dict(o, chunk_v=r.choice([0, 2048, 8192]), chunk_n=r.choice([0, 1024]))
+    return w, o
+
+
+CASES3 = [random_case_medium(i) for i in range(N_CASES3)]
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
@@ -92,6 +110,12 @@ def test_random_case_matches_oracle(i):
 def test_random_case_any_vocabulary_and_fp32_dhidden(i):
     _cuda_or_skip()
     check_case(1000 + i, *CASES2[i])
+
+
+@pytest.mark.parametrize("i", range(N_CASES3))
+def test_random_medium_case_matches_oracle(i):
+    _cuda_or_skip()
+    check_case(2000 + i, *CASES3[i])
 
 
 def check_case(i, w, o):
