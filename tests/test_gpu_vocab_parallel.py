@@ -143,24 +143,28 @@ def check_shards(w, cuts, layout, chunk_v=0):
             assert np.all(got == 0), desc
 
 
-def test_single_rank_wrapper_matches_unsharded_path():
+@pytest.mark.parametrize("V,layout", [(1024, "hv"), (1001, "vh")])
+def test_single_rank_wrapper_matches_unsharded_path(V, layout):
     """Without a process group the wrapper is one shard holding the whole vocabulary:
-    the same numbers as flce_forward / flce_backward."""
+    the same numbers as flce_forward / flce_backward (also for a [V,H] weight whose
+    vocabulary is not a multiple of 8)."""
     _cuda_or_skip()
     dev = torch.device("cuda")
-    w = dataclasses.replace(wl.TINY, name="vp4", N=256, H=128, V=1024, zloss_coef=1e-3)
+    w = dataclasses.replace(wl.TINY, name="vp4", N=256, H=128, V=V, zloss_coef=1e-3)
     hidden, weight, labels, _, _ = wl.make_inputs(w)
     h = hidden.to(dev).requires_grad_(True)
-    W = weight.to(dev).requires_grad_(True)
+    W = (weight if layout == "hv" else weight.t().contiguous()).to(dev).requires_grad_(True)
     y = labels.to(dev)
-    loss, ent = vocab_parallel_linear_cross_entropy(h, W, y, 0, w.V, "mean", zloss_coef=1e-3)
+    loss, ent = vocab_parallel_linear_cross_entropy(h, W, y, 0, w.V, "mean", zloss_coef=1e-3,
+                                                    weight_layout=layout)
     (loss + 0.25 * ent).backward()
-    ref = flce_forward(h.detach(), W.detach(), y, "mean", zloss_coef=1e-3)
+    ref = flce_forward(h.detach(), W.detach(), y, "mean", zloss_coef=1e-3,
+                       weight_layout=layout)
     assert abs(loss.item() - ref[0].item()) <= 1e-5 * abs(ref[0].item())
     assert abs(ent.item() - ref[1].item()) <= 1e-5 * abs(ref[1].item())
     dh, dw = flce_backward(h.detach(), W.detach(), y, ref[2], ref[3],
                            torch.ones(1, device=dev), torch.full((1,), 0.25, device=dev),
-                           "mean", zloss_coef=1e-3)
+                           "mean", zloss_coef=1e-3, weight_layout=layout)
     assert rel_l2(h.grad.float().cpu().numpy(), dh.float().cpu().numpy()) <= 1e-3
     assert rel_l2(W.grad.float().cpu().numpy(), dw.float().cpu().numpy()) <= 1e-3
 
