@@ -20,12 +20,18 @@ def _cuda_or_skip():
 
 
 @pytest.mark.parametrize("gif", [False, True], ids=["two_call", "grad_in_forward"])
-def test_pipeline_steps_match_direct_calls(gif):
+@pytest.mark.parametrize("layout", ["hv", "vh"])
+def test_pipeline_steps_match_direct_calls(gif, layout):
+    """[H,V] weights, and [V,H] ones with an odd vocabulary and a soft-cap."""
     _cuda_or_skip()
     base = dataclasses.replace(wl.TINY, name="p", N=700, H=256, V=1536, zloss_coef=1e-3)
+    if layout == "vh":
+        base = dataclasses.replace(base, V=1537, softcap=5.0, w_std=0.2)
     steps = [wl.make_inputs(dataclasses.replace(base, seed=s)) for s in (11, 12, 13, 14)]
-    pipe = HostPipeline(base.N, base.H, base.V, base.reduction, zloss_coef=base.zloss_coef,
-                        grad_in_forward=gif)
+    if layout == "vh":
+        steps = [(h, W.t().contiguous(), y, gl, ge) for h, W, y, gl, ge in steps]
+    kw = dict(zloss_coef=base.zloss_coef, softcap=base.softcap, weight_layout=layout)
+    pipe = HostPipeline(base.N, base.H, base.V, base.reduction, grad_in_forward=gif, **kw)
     pinned = [tuple(t.pin_memory() for t in st) for st in steps]
     got = []
     pipe.submit(*pinned[0])
@@ -41,15 +47,14 @@ def test_pipeline_steps_match_direct_calls(gif):
     dev = torch.device("cuda")
     for (h, W, y, gl, ge), (loss_h, ent_h) in zip(steps, got):
         hd, Wd, yd = h.to(dev), W.to(dev), y.to(dev)
-        loss, ent, lse, ez = flce_forward(hd, Wd, yd, base.reduction,
-                                          zloss_coef=base.zloss_coef)
+        loss, ent, lse, ez = flce_forward(hd, Wd, yd, base.reduction, **kw)
         assert torch.equal(loss.cpu(), loss_h) and torch.equal(ent.cpu(), ent_h)
     if gif:
         *_, dh, dw = flce_forward_backward(hd, Wd, yd, gl.to(dev), ge.to(dev), base.reduction,
-                                           zloss_coef=base.zloss_coef)
+                                           **kw)
     else:
         dh, dw = flce_backward(hd, Wd, yd, lse, ez, gl.to(dev), ge.to(dev), base.reduction,
-                               zloss_coef=base.zloss_coef)
+                               **kw)
     assert torch.equal(dh.view(torch.int16), dh_last.view(torch.int16))
     assert torch.equal(dw.view(torch.int16), dw_last.view(torch.int16))
 
