@@ -347,3 +347,66 @@ def test_auto_chunking_follows_the_documented_rules(lib):
         nc = max(512, (8 << 30) // (ldz * 6) // 512 * 512)
         nc = min(nc, cdiv(N, 256) * 256)
         assert flce.kernel_launches(p, 4) == 6 * cdiv(N, nc), (N, V)
+
+
+def test_random_parameter_sets_follow_the_documented_rules(lib):
+    """Seeded fuzz of flce_check_params / flce_workspace_size against the rules flce.h
+    states: random valid parameter sets pass and get a workspace for every phase; the
+    same sets with exactly one documented rule broken get that rule's status and no
+    workspace."""
+    import random
+    r = random.Random(2024)
+    OK, BAD_ARG, BAD_SHAPE, ALIGN = 0, 1, 2, 3
+
+    def valid():
+        layout = r.choice(["hv", "vh"])
+        V = r.choice([1, 7, 8, 255, 256, 1000, 50257, 128256, 1 << 20])
+        if layout == "hv":
+            V = max(8, V // 8 * 8)
+        kw = dict(N=r.choice([0, 1, 300, 8192, 1 << 20]), H=8 * r.randint(1, 1024), V=V,
+                  reduction=r.choice(["none", "mean", "sum"]),
+                  zloss_coef=r.choice([0.0, 1e-4]), softcap=r.choice([0.0, 30.0]),
+                  chunk_v=r.choice([0, 256, 65536]), weight_layout=layout,
+                  chunk_n=r.choice([0, 512, 8192]), dhidden_fp32=r.random() < 0.3)
+        if r.random() < 0.3:  # a vocabulary shard
+            kw["v_total"] = V + r.choice([0, 8, 1000])
+            kw["v_offset"] = r.randint(0, kw["v_total"] - V)
+        elif r.random() < 0.3:
+            kw["label_smoothing"] = r.choice([0.0, 0.1, 1.0])
+        return kw
+
+    breakers = [  # (rule of flce.h, how to break it, status)
+        ("H >= 8", lambda k: k.update(H=0), BAD_SHAPE),
+        ("V >= 1", lambda k: k.update(V=0), BAD_SHAPE),
+        ("N >= 0", lambda k: k.update(N=-5), BAD_SHAPE),
+        ("H % 8 == 0", lambda k: k.update(H=k["H"] + 4), ALIGN),
+        ("V % 8 == 0 for [H,V]", lambda k: k.update(weight_layout="hv", V=8 * (k["V"] // 8 + 1) + 3,
+                                                   v_total=0, v_offset=0), ALIGN),
+        ("chunk_v a multiple of 256", lambda k: k.update(chunk_v=300), BAD_ARG),
+        ("chunk_n a multiple of 512", lambda k: k.update(chunk_n=1000), BAD_ARG),
+        ("zloss_coef >= 0", lambda k: k.update(zloss_coef=-1.0), BAD_ARG),
+        ("softcap >= 0", lambda k: k.update(softcap=-2.0), BAD_ARG),
+        ("label_smoothing in [0, 1]", lambda k: k.update(label_smoothing=1.5, v_total=0,
+                                                          v_offset=0), BAD_ARG),
+        ("v_offset only with v_total", lambda k: k.update(v_total=0, v_offset=8), BAD_ARG),
+        ("shard inside the vocabulary", lambda k: k.update(v_total=k["V"], v_offset=8,
+                                                            label_smoothing=0.0), BAD_SHAPE),
+        ("no smoothing with shards", lambda k: k.update(v_total=k["V"] + 8, v_offset=0,
+                                                        label_smoothing=0.1), BAD_ARG),
+    ]
+    seen = set()
+    for _ in range(400):
+        kw = valid()
+        rule, expect = None, OK
+        if r.random() < 0.6:
+            rule, brk, expect = r.choice(breakers)
+            brk(kw)
+            seen.add(rule)
+        args = dict(kw)
+        p = flce.make_params(args.pop("N"), args.pop("H"), args.pop("V"),
+                             args.pop("reduction"), **args)
+        assert lib.flce_check_params(ctypes.byref(p)) == expect, (rule, kw)
+        for phase in (0, 1, 2):
+            n = lib.flce_workspace_size(ctypes.byref(p), phase)
+            assert (n > 0) == (expect == OK), (rule, kw, phase)
+    assert seen == {b[0] for b in breakers}
