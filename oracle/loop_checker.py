@@ -74,8 +74,10 @@ def forward_loops(hidden, weight, labels, reduction="mean", ignore_index=IGNORE_
 
 
 def objective_loops(hidden, weight, labels, g_loss, g_entropy, reduction="mean",
-                    ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0):
-    l, e, _ = forward_loops(hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap)
+                    ignore_index=IGNORE_INDEX, zloss_coef=0.0, softcap=0.0,
+                    label_smoothing=0.0, class_weight=None):
+    l, e, _ = forward_loops(hidden, weight, labels, reduction, ignore_index, zloss_coef, softcap,
+                            label_smoothing, class_weight)
     if reduction == "none":
         return sum(g * x for g, x in zip(g_loss, l)) + sum(g * x for g, x in zip(g_entropy, e))
     return g_loss[0] * l + g_entropy[0] * e

@@ -500,3 +500,40 @@ def test_extreme_logits_stay_finite():
         assert np.all(np.isfinite(dh)) and np.all(np.isfinite(dw))
         onehot = np.eye(3)[y]
         np.testing.assert_allclose(dw[0], np.eye(3)[0] - onehot, atol=1e-300)
+
+
+def _random_option_case(i):
+    import random
+    r = random.Random(600 + i)
+    N, H, V = r.randint(1, 6), r.randint(1, 5), r.randint(1, 9)
+    hidden, weight, labels = _rand_case(N, H, V, 900 + i, w_std=r.choice([0.3, 0.9, 2.0]),
+                                        ignore=tuple(r.sample(range(N), r.randint(0, N))))
+    reduction = r.choice(REDS)
+    kw = dict(zloss_coef=r.choice([0.0, 0.05]), softcap=r.choice([0.0, 1.5, 4.0]),
+              label_smoothing=r.choice([0.0, 0.0, 0.2]))
+    cw = np.random.default_rng(950 + i).uniform(0.3, 1.7, V) if r.random() < 0.4 else None
+    return hidden, weight, labels, reduction, kw, cw
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_options_oracle_against_scalar_loops(i):
+    """Seeded random tiny cases over every option at once (reduction, z-loss, soft-cap,
+    smoothing, class weights, any set of ignored rows, V down to 1): the oracle's forward
+    against the scalar loops, and its backward against central finite differences of
+    the scalar-loop objective (a second implementation, not the oracle's own)."""
+    hidden, weight, labels, reduction, kw, cw = _random_option_case(i)
+    N = hidden.shape[0]
+    out = orc.forward(hidden, weight, labels, reduction, class_weight=cw, **kw)
+    lkw = dict(kw, class_weight=None if cw is None else cw.tolist())
+    l, e, lse = lc.forward_loops(hidden.tolist(), weight.tolist(), labels.tolist(), reduction,
+                                 **lkw)
+    np.testing.assert_allclose(out["loss"], l, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out["entropy"], e, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out["lse"], lse, rtol=1e-12)
+    gl, ge = _grads(reduction, N, 600 + i)
+    dh, dw = orc.backward(hidden, weight, labels, out["lse"], out["ez"], gl, ge, reduction,
+                          class_weight=cw, **kw)
+    fh, fw = lc.fd_grads_loops(hidden.tolist(), weight.tolist(), labels.tolist(), gl.tolist(),
+                               ge.tolist(), reduction=reduction, **lkw)
+    np.testing.assert_allclose(dh, np.array(fh), rtol=1e-5, atol=1e-7)
+    np.testing.assert_allclose(dw, np.array(fw), rtol=1e-5, atol=1e-7)
