@@ -176,6 +176,12 @@ VH_ODD_VOCAB_CASES = [
                                             softcap=3.0, reduction="sum"), 256),
     ("one_class_column_past_tile", dataclasses.replace(W0, name="o4", N=64, H=16, V=257,
                                                        ignore_frac=0.0), 0),
+    # the degenerate vocabularies: one class (CE = entropy = 0; only the z-loss has a
+    # gradient) and two
+    ("single_class_zloss", dataclasses.replace(W0, name="o6", N=37, H=16, V=1,
+                                               zloss_coef=1e-2), 0),
+    ("two_classes_none", dataclasses.replace(W0, name="o7", N=300, H=24, V=2, w_std=0.5,
+                                             reduction="none", grad_mode="normal"), 0),
 ]
 
 
