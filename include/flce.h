@@ -181,7 +181,8 @@ int flce_forward_backward(const flce_params* params, const void* hidden, const v
                           void* dweight, void* workspace, size_t ws_bytes, void* stream);
 
 /* x[i] = bf16(g[0] * x[i]) for the n bf16 values at x (16-byte aligned), on
- * `stream`; the kernel returns at once when g[0] == 1.  It scales
+ * `stream`, with a zero product stored as +0 (so rows of zeros stay bitwise zero
+ * under a negative g[0]); the kernel returns at once when g[0] == 1.  It scales
  * flce_forward_backward's dhidden and dweight when the upstream gradient of the
  * loss becomes known only after the forward (autograd's backward).  Not part of
  * the pages' method: a helper of the gradient-in-forward mode. */

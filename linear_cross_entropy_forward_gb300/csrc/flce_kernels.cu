@@ -368,7 +368,8 @@ cudaError_t launch_dlogits_from_z(const float* z, int64_t rows, int64_t ldz,
   return cudaGetLastError();
 }
 
-// x *= g[0] over n bf16 values, 8 per thread (grid-stride); nothing when g[0] == 1.
+// x *= g[0] over n bf16 values, 8 per thread (grid-stride), zero products as +0;
+// nothing when g[0] == 1.
 __global__ void __launch_bounds__(256) scale_bf16_kernel(__nv_bfloat16* __restrict__ x,
                                                          int64_t n, const float* __restrict__ g) {
   const float s = *g;
@@ -383,13 +384,14 @@ __global__ void __launch_bounds__(256) scale_bf16_kernel(__nv_bfloat16* __restri
     for (int k = 0; k < 4; ++k) {
       const float lo = __uint_as_float(w[k] << 16);
       const float hi = __uint_as_float(w[k] & 0xffff0000u);
-      w[k] = pack_bf16x2(lo * s, hi * s);
+      // + 0: a zero stays +0 under a negative scale (ignored rows stay bitwise zero)
+      w[k] = pack_bf16x2(__fmaf_rn(lo, s, 0.0f), __fmaf_rn(hi, s, 0.0f));
     }
     reinterpret_cast<uint4*>(x)[i] = v;
   }
   if (blockIdx.x == 0 && threadIdx.x < n - n8 * 8) {
     const int64_t i = n8 * 8 + threadIdx.x;
-    x[i] = __float2bfloat16_rn(__bfloat162float(x[i]) * s);
+    x[i] = __float2bfloat16_rn(__fmaf_rn(__bfloat162float(x[i]), s, 0.0f));
   }
 }
 

@@ -211,6 +211,14 @@ def test_scale_bf16_matches_rounded_product(n):
     z = x.clone()
     flce_scale_bf16(z, torch.ones(1, device=dev))
     assert torch.equal(z.view(torch.int16), x.view(torch.int16))
+    # a negative scale: the product rounded the same way, zeros kept as +0
+    x[::3] = 0.0
+    ref = (x.float() * -0.37).to(torch.bfloat16)
+    ref[ref == 0] = 0.0
+    y = x.clone()
+    flce_scale_bf16(y, torch.tensor([-0.37], device=dev))
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+    assert torch.all(y[::3].view(torch.int16) == 0)
 
 
 @pytest.mark.parametrize("reduction", ["mean", "sum"])
