@@ -140,3 +140,73 @@ def test_thread_exit_with_the_backward_still_running():
         dh, dw = box["out"]
         assert torch.equal(_bits(dh), _bits(ref[0]))
         assert torch.equal(_bits(dw), _bits(ref[1]))
+
+
+def _mixed_case(i):
+    import random
+    r = random.Random(95000 + i)
+    layout = r.choice(["hv", "vh"])
+    V = r.randint(1, 6000) if layout == "vh" else 8 * r.randint(1, 750)
+    red = r.choice(["mean", "sum", "none"])
+    w = dataclasses.replace(wl.TINY, name=f"c{i}", seed=950 + i,
+                            N=r.choice([1, 37, 300, 1100, 2500]), H=8 * r.randint(1, 96), V=V,
+                            reduction=red, zloss_coef=r.choice([0.0, 1e-3]),
+                            softcap=r.choice([0.0, 5.0]),
+                            grad_mode="normal" if red == "none" else "ones")
+    h, W, y, gl, ge = wl.make_inputs(w)
+    if layout == "vh":
+        W = W.t().contiguous()
+    dev = torch.device("cuda")
+    return (w, tuple(x.to(dev) for x in (h, W, y, gl, ge)),
+            dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=layout),
+            r.random() < 0.4, r.choice([0, 256, 1024]))
+
+
+def _run_mixed(w, t, kw, gif, chunk_v):
+    hd, Wd, yd, gl, ge = t
+    if gif:
+        return flce_forward_backward(hd, Wd, yd, gl, ge, w.reduction, **kw)
+    loss, ent, lse, ez = flce_forward(hd, Wd, yd, w.reduction, **kw)
+    dh, dw = flce_backward(hd, Wd, yd, lse, ez, gl, ge, w.reduction, chunk_v=chunk_v, **kw)
+    return loss, ent, lse, ez, dh, dw
+
+
+def test_four_host_threads_with_mixed_problems():
+    """Four host threads, each on its own stream, run a shuffled mix of problems (both
+    layouts, both modes, several chunkings) twice over; every result must be bitwise
+    the one the same call gives alone (the per-device caches, side streams and tile
+    counters shared by concurrent calls must not leak between them)."""
+    _cuda_or_skip()
+    cases = [_mixed_case(i) for i in range(8)]
+    refs = [[x.clone() for x in _run_mixed(*c)] for c in cases]
+    torch.cuda.synchronize()
+    fails = []
+
+    def work(tid):
+        import random
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            order = list(range(len(cases)))
+            random.Random(tid).shuffle(order)
+            with torch.cuda.stream(s):
+                for _ in range(2):
+                    for k in order:
+                        out = _run_mixed(*cases[k])
+                        s.synchronize()
+                        for a, b in zip(out, refs[k]):
+                            if not torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16
+                                               else a,
+                                               b.view(torch.int16) if b.dtype == torch.bfloat16
+                                               else b):
+                                fails.append((tid, k))
+                                break
+        except Exception as e:  # reported in the main thread
+            fails.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not fails, fails
