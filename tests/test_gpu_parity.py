@@ -379,3 +379,45 @@ def test_schedule_counters_are_zero_after_every_call():
     f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
     assert rel_l2(f(dh), dh_o) <= GRAD_REL_L2 and rel_l2(f(dw), dw_o) <= GRAD_REL_L2
     assert rel_l2(f(out[4]), dh_o) <= GRAD_REL_L2 and rel_l2(f(out[5]), dw_o) <= GRAD_REL_L2
+
+
+def test_one_dirty_workspace_shared_by_many_problems():
+    """The workspace is scratch: one buffer, filled with a different garbage byte before
+    every use, shared by a sequence of different problems (both layouts, several
+    chunkings, both modes), gives every call the bits a fresh workspace gives."""
+    import random
+    from linear_cross_entropy_forward_gb300 import flce_forward_backward
+    _cuda_or_skip()
+    dev = torch.device("cuda")
+    big = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for i in range(12):
+        r = random.Random(97000 + i)
+        layout = r.choice(["hv", "vh"])
+        V = r.randint(1, 3000) if layout == "vh" else 8 * r.randint(1, 375)
+        gif = r.random() < 0.4
+        red = r.choice(["mean", "sum", "none"])
+        w = dataclasses.replace(W0, name=f"ws{i}", seed=970 + i, N=r.choice([1, 37, 300, 1100]),
+                                H=8 * r.randint(1, 64), V=V, reduction=red,
+                                zloss_coef=r.choice([0.0, 1e-3]), softcap=r.choice([0.0, 5.0]),
+                                grad_mode="normal" if red == "none" else "ones")
+        h, W, y, gl, ge = wl.make_inputs(w)
+        if layout == "vh":
+            W = W.t().contiguous()
+        hd, Wd, yd, gld, ged = (x.to(dev) for x in (h, W, y, gl, ge))
+        kw = dict(zloss_coef=w.zloss_coef, softcap=w.softcap, weight_layout=layout)
+        chunk_v = r.choice([0, 256])
+        results = []
+        for ws in (None, big):
+            big.fill_(r.randint(0, 255))
+            if gif:
+                results.append(flce_forward_backward(hd, Wd, yd, gld, ged, red, workspace=ws,
+                                                     **kw))
+            else:
+                f = flce_forward(hd, Wd, yd, red, workspace=ws, **kw)
+                results.append((*f, *flce_backward(hd, Wd, yd, f[2], f[3], gld, ged, red,
+                                                   chunk_v=chunk_v, workspace=ws, **kw)))
+            torch.cuda.synchronize()
+        for a, b in zip(*results):
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), (i, w, layout, gif, chunk_v)
