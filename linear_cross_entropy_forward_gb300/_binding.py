@@ -224,13 +224,17 @@ def _stream(stream):
 
 
 def _workspace(params, phase, device, workspace):
+    """The caller's workspace (checked), or a new one when none is given."""
     need = workspace_size(params, phase)
-    if workspace is not None:
-        if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 \
-                or not workspace.is_contiguous() or workspace.device != device:
-            raise TypeError(f"workspace must be a contiguous uint8 tensor on {device}")
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if workspace is None:
+        return torch.empty(need, dtype=torch.uint8, device=device)
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 \
+            or not workspace.is_contiguous() or workspace.device != device:
+        raise TypeError(f"workspace must be a contiguous uint8 tensor on {device}")
+    if workspace.numel() < need:
+        # never a silent allocation behind a caller that passes its own memory
+        raise ValueError(f"workspace holds {workspace.numel()} bytes; this call needs {need} "
+                         f"(workspace_size(params, {phase}))")
     return workspace
 
 

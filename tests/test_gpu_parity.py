@@ -335,6 +335,9 @@ def test_binding_rejects_mismatched_outputs_and_workspace():
         flce_forward(hidden, weight, labels, "none", out=good[:3])
     with pytest.raises(TypeError):  # workspace not bytes
         flce_forward(hidden, weight, labels, "none", workspace=torch.empty(1 << 20, **f32))
+    with pytest.raises(ValueError):  # a workspace too small is refused, not replaced
+        flce_forward(hidden, weight, labels, "none",
+                     workspace=torch.empty(256, dtype=torch.uint8, device=dev))
     dh = torch.empty(64, 64, dtype=torch.bfloat16, device=dev)
     with pytest.raises(ValueError):  # dweight shaped like dhidden
         flce_backward(hidden, weight, labels, good[2], good[3], None, None, "none",
