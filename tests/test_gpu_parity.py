@@ -141,6 +141,12 @@ CASES = [
     # forward partials to merge, column indices past 2^21 in every kernel
     ("vocab_2m", dataclasses.replace(W0, name="v2m", N=130, H=64, V=2 ** 21 + 264,
                                      zloss_coef=1e-3), 0),
+    # the other extremes: a 16384-wide hidden (256 k-blocks per output tile) and 100000
+    # rows (391 row tiles) over a narrow vocabulary
+    ("hidden_16k", dataclasses.replace(W0, name="x1", N=300, H=16384, V=1000, w_std=0.004,
+                                       reduction="none", grad_mode="normal"), 0),
+    ("rows_100k", dataclasses.replace(W0, name="x2", N=100000, H=64, V=264, w_std=0.1,
+                                      zloss_coef=1e-3), 256),
 ]
 
 
