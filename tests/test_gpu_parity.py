@@ -294,6 +294,41 @@ def test_bad_label_reported():
     assert ei.value.code == 5
 
 
+def test_bad_labels_flag_only_their_rows():
+    """Labels outside [0, V) that are not ignore_index (past V, far past it, negative):
+    without validate the call still completes, the workspace's status reports
+    FLCE_ERR_LABEL, those rows' loss and entropy are NaN, and every other output (the
+    other rows' loss and entropy, every row's lse and E_p[z]) matches the oracle."""
+    _cuda_or_skip()
+    from linear_cross_entropy_forward_gb300 import flce_status, make_params, workspace_size
+    w = dataclasses.replace(W0, name="bl", N=300, H=64, V=1000, reduction="none",
+                            grad_mode="normal")
+    hidden, weight, labels, _, _ = wl.make_inputs(w)
+    bad_rows = [3, 77, 150, 151, 299]
+    bad = labels.clone()
+    for r_, v in zip(bad_rows, [w.V, w.V + 7, -5, -101, 1 << 40]):
+        bad[r_] = v
+    dev = torch.device("cuda")
+    ws = torch.empty(workspace_size(make_params(w.N, w.H, w.V, "none"), 0), dtype=torch.uint8,
+                     device=dev)
+    loss, ent, lse, ez = flce_forward(hidden.to(dev), weight.to(dev), bad.to(dev), "none",
+                                      workspace=ws)
+    assert flce_status(ws) == 5
+    h = orc.bf16_bits_to_f64(wl.bf16_bits(hidden))
+    W = orc.bf16_bits_to_f64(wl.bf16_bits(weight))
+    masked = bad.numpy().copy()
+    masked[bad_rows] = orc.IGNORE_INDEX
+    o = orc.forward(h, W, masked, "none")
+    f = lambda t: t.cpu().numpy().astype(np.float64)  # noqa: E731
+    good = np.ones(w.N, bool)
+    good[bad_rows] = False
+    assert np.all(np.isnan(f(loss)[bad_rows])) and np.all(np.isnan(f(ent)[bad_rows]))
+    assert np.abs(f(loss)[good] - o["loss"][good]).max() <= TOK_ABS
+    assert np.abs(f(ent)[good] - o["entropy"][good]).max() <= TOK_ABS
+    assert np.abs(f(lse) - o["lse"]).max() <= TOK_ABS
+    assert np.abs(f(ez) - o["ez"]).max() <= TOK_ABS
+
+
 def test_deterministic_repeat():
     _cuda_or_skip()
     w = dataclasses.replace(W0, name="d1", N=300, H=200, V=1000, zloss_coef=1e-3)
