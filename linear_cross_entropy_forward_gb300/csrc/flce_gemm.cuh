@@ -743,6 +743,16 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     if (lane == 0 && prank == 0) {
       // ---------------- UMMA issuer (pair leaders only)
       constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_BM, TN, A_MN, B_MN);
+      // Shared-memory descriptors of stage 0, k-slice 0, computed once: the start-address
+      // field (bits 0-13, address >> 4; every address here is below 2^18) then advances by a
+      // stage's bytes >> 4 and a k-slice's offset >> 4.  Rebuilding all eight descriptors
+      // every k-block kept the UMMA thread busy enough that, with the epilogue's arithmetic
+      // beside it on the SM, the tensor pipe starved: the soft-capped Gemma-2 forward lost
+      // twice the cycles.
+      const uint64_t a_desc0 = operand_desc<A_MN>(smem_u32(sA), 0, sh);
+      const uint64_t b_desc0 = operand_desc<B_MN>(smem_u32(sB), 0, sh);
+      constexpr uint64_t kKA = (A_MN ? UK * 128 : UK * 2) >> 4;
+      constexpr uint64_t kKB = (B_MN ? UK * 128 : UK * 2) >> 4;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -759,13 +769,13 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
+          const uint64_t a_st = a_desc0 + stage * (C::A_BYTES >> 4);
+          const uint64_t b_st = b_desc0 + stage * (C::B_BYTES >> 4);
           uint64_t ad[BK / UK], bd[BK / UK];
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            ad[kk] = operand_desc<A_MN>(a_addr, kk, sh);
-            bd[kk] = operand_desc<B_MN>(b_addr, kk, sh);
+            ad[kk] = a_st + kk * kKA;
+            bd[kk] = b_st + kk * kKB;
           }
           umma_bf16_pair_x4(d_tmem, ad, bd, IDESC, kb != 0 ? 1u : 0u);
           umma_commit_pair(&empty[stage], kPairMask);
