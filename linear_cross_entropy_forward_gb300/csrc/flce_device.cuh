@@ -274,7 +274,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile
 // (Blackwell format: start>>4 in [0,14), LBO>>4 in [16,30), SBO>>4 in [32,46),
 // version 1 at bit 46, swizzle mode 2 = 128B at bits [61,64)).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+__host__ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
                                                 uint32_t sbo_bytes) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);

@@ -246,7 +246,8 @@ __device__ __forceinline__ bool load_operand(uint8_t* dst, const CUtensorMap* ma
 }
 
 template <bool MN>
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, const GemmShape& sh) {
+__host__ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk,
+                                                          const GemmShape& sh) {
   if constexpr (!MN) {
     // K-major: the k-th 16-element slice starts 32 bytes further into each
     // 128-byte swizzled row; 8-row groups are 1024 bytes apart.

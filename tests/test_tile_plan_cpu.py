@@ -139,3 +139,61 @@ def test_tile_order_covers_every_tile_once(tmp_path):
     assert r.returncode == 0, r.stderr[-3000:]
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
+
+
+DESC_CHECK = r"""
+#include <cstdio>
+#include "flce_gemm.cuh"
+using namespace flce;
+
+// The UMMA thread builds each stage's descriptors by adding (stage bytes >> 4) and
+// (k-slice offset >> 4) to the stage-0, k-slice-0 descriptor: that must equal building
+// them from the addresses, for every stage and k-slice, at every shared-memory base the
+// kernel's operand rings can have (1 KB aligned, the ring inside the 2^18-byte window).
+template <bool MN, int BYTES>
+static int check(const GemmShape& sh) {
+  constexpr int STAGES = PairCfg<256, 4>::STAGES;
+  constexpr uint64_t kK = (MN ? UK * 128 : UK * 2) >> 4;
+  for (uint32_t base = 0; base + STAGES * BYTES <= (1u << 18); base += 1024) {
+    const uint64_t d0 = operand_desc<MN>(base, 0, sh);
+    for (int s = 0; s < STAGES; ++s)
+      for (int kk = 0; kk < BK / UK; ++kk)
+        if (operand_desc<MN>(base + s * BYTES, kk, sh) !=
+            d0 + static_cast<uint64_t>(s) * (BYTES >> 4) + kk * kK)
+          return 1;
+  }
+  return 0;
+}
+
+int main() {
+  GemmShape sh{};
+  sh.mn_lbo = MN_ATOM_BYTES;
+  sh.mn_sbo = 1024;
+  using C = PairCfg<256, 4>;
+  const int rc = check<false, C::A_BYTES>(sh) | check<true, C::A_BYTES>(sh) |
+                 check<false, C::B_BYTES>(sh) | check<true, C::B_BYTES>(sh);
+  std::printf(rc ? "FAIL\n" : "OK\n");
+  return rc;
+}
+"""
+
+
+def test_incremental_descriptors_equal_rebuilt_ones(tmp_path):
+    """The shared-memory descriptors the UMMA thread advances by stage and k-slice equal
+    the ones built from the operand addresses (compiled for the host with nvcc)."""
+    import os
+    import subprocess
+    from linear_cross_entropy_forward_gb300.build import CSRC, ROOT, nvcc_path
+    try:
+        nvcc = nvcc_path()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    src = tmp_path / "desc_check.cu"
+    src.write_text(DESC_CHECK)
+    exe = tmp_path / "desc_check"
+    r = subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                        "-I" + CSRC, "-I" + os.path.join(ROOT, "include"), str(src), "-o",
+                        str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
